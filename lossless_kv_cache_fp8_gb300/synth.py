@@ -1,0 +1,173 @@
+"""Seeded synthetic inputs shaped like the pages' workloads.
+
+This module only draws random numbers; it holds none of the codec's
+arithmetic, so both the CUDA path and the CPU oracle consume the same bytes
+from it.  The speculative-KV-coding page measured real Qwen3 KV caches
+("early results"); those caches, models and prompts are not available, so
+seeded caches with the same shapes stand in for them:
+
+* KV caches ``[layer][k/v][kv_head][token][head_dim]``: per-channel scale
+  ``sigma_c = exp(U(ln 0.1, ln 2))``, 2% of channels (chosen by the seed) 10x
+  larger; ``x ~ N(0, sigma_c)``; target = cast(x); predictor =
+  cast(x + eps) with ``eps ~ Laplace(0, eps_scale * sigma_c)`` (0.05 for FP8,
+  0.01 for BF16).  The cast is round-to-nearest-even (torch).
+* Transform-coefficient stream ``[token][coef]`` (the DCKV page's setting):
+  ``b_c = exp(U(ln 0.3, ln 20))``, step ``Delta_c = exp(U(0, ln 32))``,
+  mean ``mu'_{t,c} ~ N(0, (4 b_c)^2)``, ``y ~ Laplace(mu', b_c)``,
+  ``q = clamp(rint(y / Delta_c), +-32767)``; the coder receives
+  ``mu = mu' / Delta_c`` (fp32) and ``beta_c = b_c / Delta_c`` (fp32);
+  components with ``beta_c < 0.05`` are switched off and their q set to 0.
+
+Random draws use torch generators (a CPU generator for per-channel
+parameters, the tensor's device generator for the bulk).  Bytes drawn on one
+device are copied, never regenerated, when the other side needs them.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+FP8, BF16, COEF = 1, 2, 3
+BASE_SEED = 20261202
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    dtype: int
+    n_layers: int = 0
+    n_kv: int = 2
+    n_heads: int = 8
+    head_dim: int = 128
+    n_tokens: int = 0
+    n_coef: int = 0
+    lane_syms: int = 1024
+    n_calib: int = 256
+    eps_scale: float = 0.05
+    index: int = 0
+
+    @property
+    def seed(self) -> int:
+        return BASE_SEED + self.index
+
+    @property
+    def elem_bytes(self) -> int:
+        return 1 if self.dtype == FP8 else 2
+
+    @property
+    def n_positions(self) -> int:
+        if self.dtype == COEF:
+            return self.n_tokens * self.n_coef
+        return self.n_layers * self.n_kv * self.n_heads * self.n_tokens * self.head_dim
+
+    @property
+    def raw_bytes(self) -> int:
+        """bytes of the cache being coded (the target)"""
+        return self.n_positions * self.elem_bytes
+
+    def shape(self):
+        if self.dtype == COEF:
+            return (self.n_tokens, self.n_coef)
+        return (self.n_layers, self.n_kv, self.n_heads, self.n_tokens, self.head_dim)
+
+    def scaled(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+# The five workloads: Qwen3-0.6B / 8B / 32B KV shapes (8 KV heads, head_dim 128) and a
+# hybrid model's coefficient stream (32768 tokens x 2048 coefficients).
+WORKLOADS = {
+    "qwen3-0.6b-1k-fp8": Workload("qwen3-0.6b-1k-fp8", FP8, n_layers=28, n_tokens=1024,
+                                  lane_syms=1024, eps_scale=0.05, index=0),
+    "qwen3-0.6b-8k-bf16": Workload("qwen3-0.6b-8k-bf16", BF16, n_layers=28, n_tokens=8192,
+                                   lane_syms=1024, eps_scale=0.01, index=1),
+    "qwen3-8b-32k-fp8": Workload("qwen3-8b-32k-fp8", FP8, n_layers=36, n_tokens=32768,
+                                 lane_syms=4096, eps_scale=0.05, index=2),
+    "qwen3-32b-128k-fp8": Workload("qwen3-32b-128k-fp8", FP8, n_layers=64, n_tokens=131072,
+                                   lane_syms=4096, eps_scale=0.05, index=3),
+    "hybrid-coef-32k-x2048": Workload("hybrid-coef-32k-x2048", COEF, n_tokens=32768, n_coef=2048,
+                                      lane_syms=1024, n_calib=0, index=4),
+}
+WORKLOAD_ORDER = list(WORKLOADS)
+
+
+def _laplace(shape, scale, gen, device):
+    u = torch.rand(shape, generator=gen, device=device, dtype=torch.float32) - 0.5
+    a = u.abs().clamp_(max=0.5 - 2.0 ** -25)
+    return -scale * torch.sign(u) * torch.log1p(-2.0 * a)
+
+
+def _cast_bits(v: torch.Tensor, dtype: int) -> torch.Tensor:
+    if dtype == FP8:
+        return v.to(torch.float8_e4m3fn).view(torch.uint8)
+    return v.to(torch.bfloat16).view(torch.int16)
+
+
+def channel_sigma(w: Workload) -> torch.Tensor:
+    """per-channel scale sigma_c, [layer][kv][head][head_dim] on the CPU"""
+    g = torch.Generator().manual_seed(w.seed)
+    shp = (w.n_layers, w.n_kv, w.n_heads, w.head_dim)
+    n = math.prod(shp)
+    u = torch.rand(n, generator=g, dtype=torch.float64)
+    sig = torch.exp(math.log(0.1) + u * (math.log(2.0) - math.log(0.1)))
+    n_out = max(1, round(0.02 * n))
+    idx = torch.randperm(n, generator=g)[:n_out]
+    sig[idx] *= 10.0
+    return sig.view(shp).to(torch.float32)
+
+
+def gen_kv(w: Workload, device="cpu", layers=None):
+    """(target_bits, pred_bits): uint8 (FP8) or int16 (BF16 bit patterns) tensors of
+    shape [layer][kv][head][token][head_dim] on `device`.  `layers` restricts the
+    draw to a range of layers (same values as the full draw)."""
+    assert w.dtype in (FP8, BF16)
+    sig = channel_sigma(w)
+    lo, hi = (0, w.n_layers) if layers is None else layers
+    tdt = torch.uint8 if w.dtype == FP8 else torch.int16
+    shp = (hi - lo, w.n_kv, w.n_heads, w.n_tokens, w.head_dim)
+    target = torch.empty(shp, dtype=tdt, device=device)
+    pred = torch.empty(shp, dtype=tdt, device=device)
+    for li in range(lo, hi):
+        # one generator per layer so that any layer range reproduces the full draw
+        g = torch.Generator(device=device).manual_seed(w.seed * 1000003 + li)
+        s = sig[li].to(device).view(w.n_kv, w.n_heads, 1, w.head_dim)
+        x = torch.randn((w.n_kv, w.n_heads, w.n_tokens, w.head_dim), generator=g,
+                        device=device, dtype=torch.float32) * s
+        eps = _laplace(x.shape, w.eps_scale * s, g, device)
+        target[li - lo] = _cast_bits(x, w.dtype)
+        pred[li - lo] = _cast_bits(x + eps, w.dtype)
+        del x, eps
+    return target, pred
+
+
+def gen_coef(w: Workload, device="cpu"):
+    """(q int16 [T][C], mu fp32 [T][C], beta fp32 [C]) on `device`."""
+    assert w.dtype == COEF
+    g = torch.Generator().manual_seed(w.seed)
+    C = w.n_coef
+    b = torch.exp(math.log(0.3) + torch.rand(C, generator=g, dtype=torch.float64)
+                  * (math.log(20.0) - math.log(0.3))).to(torch.float32)
+    delta = torch.exp(torch.rand(C, generator=g, dtype=torch.float64) * math.log(32.0)).to(torch.float32)
+    beta = b / delta
+    gd = torch.Generator(device=device).manual_seed(w.seed * 1000003 + 7)
+    bd, dd = b.to(device), delta.to(device)
+    mu_y = torch.randn((w.n_tokens, C), generator=gd, device=device, dtype=torch.float32) * (4.0 * bd)
+    y = mu_y + _laplace(mu_y.shape, bd, gd, device)
+    q = torch.round(y / dd).clamp_(-32767, 32767).to(torch.int16)
+    mu = (mu_y / dd).to(torch.float32)
+    off = ~(beta >= 0.05)
+    q[:, off.to(device)] = 0
+    return q, mu, beta.to(device)
+
+
+def gen_workload(w: Workload, device="cpu"):
+    """Uniform entry: returns (target, pred, calib_pred) where calib_pred is the
+    second input of calibration (the predictor cache for KV, beta for COEF) and
+    pred is the second input of encode/decode (the predictor cache, or mu)."""
+    if w.dtype == COEF:
+        q, mu, beta = gen_coef(w, device)
+        return q, mu, beta
+    t, p = gen_kv(w, device)
+    return t, p, p
