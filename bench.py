@@ -1,0 +1,375 @@
+"""Benchmark: speculative KV coding round trip on one GB300.
+
+One step = the whole hot path over one cache: calibrate (per-channel Laplace
+scales), build tables, encode (rANS lanes, scan, pack), decode (fused
+reconstruction).  Inputs are resident in HBM before the timed region; the
+128K-token Qwen3-32B-shaped FP8 cache (2 x 17.2 GB) is far larger than L2, so no
+flush is needed between steps.
+
+Prints one JSON line.  ``value`` = raw target-cache bytes per step / step time
+(GB/s, whole job).  ``e2e`` repeats the step through the same C ABI with the
+inputs copied from pinned host memory and the bitstream copied back inside the
+timed region.  ``--impl reference`` times the CPU oracle (the reference arm of
+this method) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV codec GB/s (raw KV in) enc/dec, Qwen3-32B shape 128K, % of HBM peak; ratio"
+DEFAULT_WORKLOAD = "qwen3-32b-128k-fp8"
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return None
+
+
+def hbm_peak():
+    pk = peaks()
+    if pk and pk.get("hbm_gbs"):
+        return float(pk["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region"""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "samples": len(rows), "reasons": reasons}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world, device):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------------
+# reference arm: the CPU oracle on a bounded sample of the workload
+# ------------------------------------------------------------------------------------------
+def oracle_sample(w, n_slices: int):
+    """first n_slices (layer, kv, head) slices of the workload, generated on the CPU"""
+    from lossless_kv_cache_fp8_gb300 import synth
+    per_layer = w.n_kv * w.n_heads
+    n_layers = (n_slices + per_layer - 1) // per_layer
+    t, p = synth.gen_kv(w, "cpu", layers=(0, n_layers))
+    sp = w.n_tokens * w.head_dim
+    t = t.reshape(-1)[: n_slices * sp].numpy()
+    p = p.reshape(-1)[: n_slices * sp].numpy()
+    if w.dtype != synth.FP8:
+        t, p = t.view("uint16"), p.view("uint16")
+    return t, p
+
+
+def run_oracle_round_trip(w, t, p, n_slices):
+    """calibrate + tables + encode + decode of n_slices slices with the oracle; returns seconds"""
+    import numpy as np
+    import oracle
+    oracle.build()
+    # n_slices slices as a cache of n_slices heads
+    po = oracle.kv_params(w.dtype, 1, 1, n_slices, w.head_dim, w.n_tokens, w.lane_syms, w.n_calib)
+    t0 = time.perf_counter()
+    bins, _, _ = oracle.calibrate(po, t, p, want_sum=False)
+    fr, cum = oracle.build_tables(po)
+    st, bs, offs = oracle.encode(po, fr, cum, bins, t, p)
+    st2, out = oracle.decode(po, fr, cum, bins, bs, offs, p, t.dtype)
+    dt = time.perf_counter() - t0
+    assert st == oracle.OK and st2 == oracle.OK and np.array_equal(out, t)
+    return dt, bs.size
+
+
+def cpu_baseline(w, target_seconds=12.0):
+    """oracle round trip on the first slices of the workload, about target_seconds of CPU"""
+    t, p = oracle_sample(w, 1)
+    dt1, _ = run_oracle_round_trip(w, t, p, 1)
+    n = max(1, min(w.n_layers * w.n_kv * w.n_heads, int(target_seconds / max(dt1, 1e-3))))
+    if n > 1:
+        t, p = oracle_sample(w, n)
+        dt, _ = run_oracle_round_trip(w, t, p, n)
+    else:
+        dt = dt1
+    raw = t.nbytes
+    return {"value": raw / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {n} of {w.n_layers * w.n_kv * w.n_heads} (layer,kv,head) slices "
+                      f"({raw / 1e6:.1f} MB raw KV), single-threaded calibrate+tables+encode+decode"}
+
+
+def main_reference(args):
+    from lossless_kv_cache_fp8_gb300 import synth
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return
+    w = synth.WORKLOADS[args.workload]
+    n_slices = max(1, args.ref_slices)
+    t, p = oracle_sample(w, n_slices)
+    for _ in range(args.warmup):
+        run_oracle_round_trip(w, t, p, n_slices)
+    times = []
+    for _ in range(args.steps):
+        dt, _ = run_oracle_round_trip(w, t, p, n_slices)
+        times.append(dt)
+    total = sum(times)
+    raw = t.nbytes
+    v = raw * len(times) / total / 1e9
+    sample = (f"first {n_slices} of {w.n_layers * w.n_kv * w.n_heads} (layer,kv,head) slices "
+              f"({raw / 1e6:.1f} MB raw KV) per step, single-threaded")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u8" if w.dtype == synth.FP8 else "u16", "data": "synthetic",
+        "config": {"workload": w.name, "sample": sample},
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------
+def main_ours(args):
+    import torch
+    from lossless_kv_cache_fp8_gb300 import build as libbuild
+    from lossless_kv_cache_fp8_gb300 import native, synth
+
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    libbuild.build()
+    w = synth.WORKLOADS[args.workload]
+    p = native.params_for(w)
+    sz = native.sizes(p)
+    stream = torch.cuda.current_stream(dev)
+
+    # inputs resident in HBM before the timed region
+    tgt, prd, cal = synth.gen_workload(w, dev)
+    codec = native.Codec(p, device=dev, bitstream_capacity=int(w.raw_bytes * args.cap_frac))
+    out = torch.empty_like(tgt)
+    torch.cuda.synchronize()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        codec.calibrate(None if w.dtype == synth.COEF else tgt, cal)
+        if ev:
+            ev[1].record(stream)
+        codec.build_tables()
+        if ev:
+            ev[2].record(stream)
+        codec.encode(tgt, prd, want_total=False)
+        if ev:
+            ev[3].record(stream)
+        codec.decode(prd, out, n_bytes=step.n_bytes)   # same stream every step (deterministic)
+        if ev:
+            ev[4].record(stream)
+
+    # first pass: sizes, correctness
+    codec.calibrate(None if w.dtype == synth.COEF else tgt, cal)
+    codec.build_tables()
+    total = codec.encode(tgt, prd, want_total=True)
+    st = codec.check()
+    assert st == native.SKV_OK, native.status_string(st)
+    step.n_bytes = total
+    codec.decode(prd, out, n_bytes=total)
+    assert codec.check() == native.SKV_OK and torch.equal(out, tgt), "round trip failed"
+
+    for _ in range(args.warmup):
+        step(ev=[torch.cuda.Event(enable_timing=True) for _ in range(5)])
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for k in range(args.steps):
+            step(ev=evs[k])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    st = codec.check()
+    assert st == native.SKV_OK, native.status_string(st)
+    ms = t_start.elapsed_time(t_end) / args.steps
+    ms = max_over_ranks(ms, world, dev)
+    phase = {name: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
+             for i, name in enumerate(["calibrate", "build_tables", "encode", "decode"])}
+
+    peak, peak_kind = hbm_peak()
+    raw = w.raw_bytes
+    pred_bytes = w.n_positions * (4 if w.dtype == synth.COEF else w.elem_bytes)
+    lanes = sz["lanes"]
+    enc_bytes = raw + pred_bytes + total + 8 * (lanes + 1)           # in: both caches; out: stream + offsets
+    dec_bytes = pred_bytes + total + 8 * (lanes + 1) + raw           # in: pred + stream + offsets; out: target
+    enc_gbs = enc_bytes / phase["encode"] / 1e6
+    dec_gbs = dec_bytes / phase["decode"] / 1e6
+    dominant = "decode" if phase["decode"] >= phase["encode"] else "encode"
+    achieved = dec_gbs if dominant == "decode" else enc_gbs
+    stored = total + 4 * lanes + sz["channels"] + 64
+    value = raw * world / (ms * 1e-3) / 1e9
+
+    res = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u8" if w.dtype == synth.FP8 else ("u16" if w.dtype == synth.BF16 else "i16"),
+        "data": "synthetic",
+        "config": {"workload": w.name, "shape": list(w.shape()), "lane_syms": w.lane_syms,
+                   "l2": "inputs larger than L2 (no flush)",
+                   "step": "calibrate + build_tables + encode + decode"},
+        "phases_ms": phase,
+        "encode_raw_gbs": raw / phase["encode"] / 1e6, "decode_raw_gbs": raw / phase["decode"] / 1e6,
+        "encode_total_gbs": enc_gbs, "decode_total_gbs": dec_gbs,
+        "encode_hbm_frac": enc_gbs / peak, "decode_hbm_frac": dec_gbs / peak,
+        "ratio": raw / stored, "bitstream_bytes": total,
+        "roofline": {"bound": "hbm", "kernel": f"skv_{dominant}", "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": None},
+        "gpu_launches": 8 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if args.e2e and world >= 1:
+        res["e2e"] = e2e(args, w, codec, tgt, prd, cal, out, stream, dev, total)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+def e2e(args, w, codec, tgt, prd, cal, out, stream, dev, total):
+    """same step through the C ABI, inputs from pinned host memory, bitstream read back"""
+    import torch
+    from lossless_kv_cache_fp8_gb300 import synth
+    try:
+        h_t = torch.empty(tgt.shape, dtype=tgt.dtype, pin_memory=True)
+        h_p = torch.empty(prd.shape, dtype=prd.dtype, pin_memory=True)
+        h_bs = torch.empty(int(total * 1.05) + 4096, dtype=torch.uint8, pin_memory=True)
+    except RuntimeError as e:
+        return {"value": None, "unit": "GB/s", "error": f"pinned host allocation failed: {e}"[:200]}
+    h_t.copy_(tgt)
+    h_p.copy_(prd)
+    h_off = torch.empty(codec.lane_offsets.shape, dtype=torch.int64, pin_memory=True)
+    torch.cuda.synchronize()
+    times = []
+    nb = 0
+    for k in range(args.warmup + max(1, args.e2e_steps)):
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        tgt.copy_(h_t, non_blocking=True)
+        prd.copy_(h_p, non_blocking=True)
+        codec.calibrate(None if w.dtype == synth.COEF else tgt, cal)
+        codec.build_tables()
+        n = codec.encode(tgt, prd, want_total=True)
+        h_bs[:n].copy_(codec.bitstream[:n], non_blocking=True)
+        h_off.copy_(codec.lane_offsets, non_blocking=True)
+        codec.decode(prd, out, n_bytes=n)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        if k >= args.warmup:
+            times.append(t0.elapsed_time(t1))
+        nb = n
+    assert torch.equal(out, tgt)
+    ms = statistics.mean(times)
+    h2d = h_t.numel() * h_t.element_size() + h_p.numel() * h_p.element_size()
+    d2h = nb + h_off.numel() * 8
+    return {"value": w.raw_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": len(times)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cap-frac", type=float, default=0.6, help="bitstream buffer / raw bytes")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-slices", type=int, default=2, help="reference arm: slices per step")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        main_reference(args)
+    else:
+        main_ours(args)
+
+
+if __name__ == "__main__":
+    main()

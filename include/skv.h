@@ -1,0 +1,189 @@
+/*
+ * skv.h -- C ABI of the GB300 speculative-KV-coding library (libskv.so).
+ *
+ * Lossless coding of a target model's KV cache against a predictor's
+ * approximation of it.  Sources (page title, section):
+ *   [SKV]  "Speculative KV coding: losslessly compressing KV cache by up to ~4x"
+ *          (summary at aisparkup.com/posts/13411), sections "core idea" and
+ *          "which predictor".
+ *   [DCKV] "DCKV compresses a hybrid language model's prompt KV cache with
+ *          learned transform coding" (onedev.kr/papers/1428), sections "how it
+ *          works", "how it differs" and "usage".
+ *
+ * Conventions for every call:
+ *   - Pointers prefixed d_ are device memory owned by the caller; h_ pointers
+ *     are host memory.  The library allocates nothing and frees nothing.
+ *   - Device buffers must be 16-byte aligned (cudaMalloc gives 256).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls enqueue their kernels on it and return without waiting,
+ *     except where a call says it synchronises.
+ *   - Argument errors are reported synchronously (SKV_ERR_INVALID_ARG or
+ *     SKV_ERR_UNSUPPORTED) before anything is launched.  Launch failures give
+ *     SKV_ERR_CUDA.  Errors found by kernels while they run (a corrupt stream,
+ *     too small an output buffer, an out-of-range bin) are recorded in a
+ *     caller-owned 32-bit device status word and read with skv_read_status.
+ *   - Kernels never trap; a bad stream gives a status, never a fault.
+ *
+ * Data layouts:
+ *   KV cache (FP8 E4M3 or BF16 bit patterns): [layer][kv][head][token][head_dim],
+ *     row-major.  Channel c = ((layer*n_kv + kv)*n_heads + head)*head_dim + d.
+ *   Coefficient stream (COEF): q int16 [token][coef], row-major; means mu fp32
+ *     [token][coef] (in quantisation-step units); scales beta fp32 [coef].
+ *
+ * Stream format (what the oracle reproduces byte for byte):
+ *   A slice is one (layer, kv, head) block of n_tokens*head_dim positions
+ *   (COEF: the whole [token][coef] grid).  Each slice is cut into chunks of
+ *   32*lane_syms positions (the last one may be short).  Positions come in
+ *   groups of 16 bytes (16 FP8 values, 8 BF16 or COEF values); lane l of a
+ *   chunk owns the groups whose chunk-local index is l mod 32.  Each lane is an
+ *   independent rANS stream with a 32-bit state in [2^16, 2^32), 16-bit
+ *   renormalisation and 12-bit probabilities ([DCKV] how it differs: GPU rANS
+ *   over Laplace-integrated probabilities), coded backwards:
+ *     lane words (u16, little endian) = [x_final >> 16, x_final & 0xFFFF,
+ *                                        renormalisation words, last first]
+ *   Symbols: residual r = ord(target) - ord(pred) of monotone ordinals
+ *   ([SKV] core idea); |r| <= 127 -> symbol r + 127, otherwise the escape
+ *   symbol 255 followed by the residual mod 2^width as raw bytes (uniform
+ *   steps of frequency 16, high byte decoded first).  COEF: r = q - floor(mu'),
+ *   mu' = mu rounded to 1/16, and components with beta < 0.05 carry no
+ *   symbols ([DCKV] how it works) and decode to 0.
+ *   Lanes are stored in lane order (chunk*32 + l); lane_offsets[g] is the
+ *   byte offset of lane g and lane_offsets[n_lanes] the total size.
+ */
+#ifndef SKV_H
+#define SKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SKV_PARAMS_VERSION 1u
+
+/* status codes */
+#define SKV_OK 0
+#define SKV_ERR_INVALID_ARG 1
+#define SKV_ERR_CUDA 2
+#define SKV_ERR_CAPACITY 3
+#define SKV_ERR_CORRUPT 4
+#define SKV_ERR_TIMEOUT 5
+#define SKV_ERR_UNSUPPORTED 6
+
+/* dtype codes */
+#define SKV_FP8_E4M3 1u
+#define SKV_BF16 2u
+#define SKV_COEF_I16 3u
+
+/* Table blob: table t occupies SKV_TABLE_STRIDE bytes at t*SKV_TABLE_STRIDE.
+ * Within a table:
+ *   SKV_TABLE_ENC_OFF  256 x {u32 m_lo, u32 m_hi, u32 fr<<20, u32 (4096-fr) | cum<<16}
+ *                      encoder entries; floor(x/fr) = (umulhi(x,m_lo) + x*m_hi) >> 12
+ *                      with m = ceil(2^44/fr), exact for every state the coder meets
+ *   SKV_TABLE_LUT_OFF  4096 x u8: symbol owning each 12-bit slot
+ *   SKV_TABLE_DEC_OFF  256 x u32: fr | cum << 16
+ *   SKV_TABLE_FREQ_OFF 256 x u16: frequencies (sum 4096, each >= 1)
+ *   SKV_TABLE_CUM_OFF  257 x u16: cumulative frequencies (cum[256] = 4096)
+ * KV streams have 32 tables (scale bin b = table b); COEF streams have 1024
+ * (table 16*b + f: scale bin b, mean fraction f/16). */
+#define SKV_TABLE_STRIDE 12288u
+#define SKV_TABLE_ENC_OFF 0u
+#define SKV_TABLE_LUT_OFF 4096u
+#define SKV_TABLE_DEC_OFF 8192u
+#define SKV_TABLE_FREQ_OFF 9216u
+#define SKV_TABLE_CUM_OFF 9728u
+
+/* Status-word bits set by kernels (skv_read_status maps them to codes). */
+#define SKV_FLAG_CORRUPT 1u
+#define SKV_FLAG_CAPACITY 2u
+#define SKV_FLAG_TIMEOUT 4u
+#define SKV_FLAG_BAD_BIN 8u
+
+typedef struct {
+  uint32_t version;   /* SKV_PARAMS_VERSION                                     */
+  uint32_t dtype;     /* SKV_FP8_E4M3, SKV_BF16 or SKV_COEF_I16                 */
+  uint32_t n_layers;  /* KV only                                                */
+  uint32_t n_kv;      /* KV only: 2 for {K, V}                                  */
+  uint32_t n_heads;   /* KV only: KV heads                                      */
+  uint32_t head_dim;  /* KV only: multiple of 16 (FP8) / 8 (BF16) dividing 512 / 256 */
+  uint64_t n_tokens;
+  uint32_t n_coef;    /* COEF only: coefficients per token                      */
+  uint32_t lane_syms; /* positions per lane (chunk = 32 lanes); a multiple of
+                         the group size (16 FP8, 8 otherwise), at most 65536    */
+  uint32_t n_calib;   /* KV only: calibration tokens per channel (<= 65536)     */
+  uint32_t reserved;  /* must be 0                                              */
+} skv_params;
+
+/* Text for a status code (static storage). */
+const char* skv_status_string(int status);
+
+/* SKV_OK if the parameters describe a supported stream, else
+ * SKV_ERR_INVALID_ARG / SKV_ERR_UNSUPPORTED.  Host only. */
+int skv_check_params(const skv_params* p);
+
+/* Sizes (host only; 0 for invalid parameters). */
+uint64_t skv_num_positions(const skv_params* p); /* values in the target          */
+uint64_t skv_num_channels(const skv_params* p);  /* entries of the bins array      */
+uint32_t skv_num_tables(const skv_params* p);    /* 32 (KV) or 1024 (COEF)         */
+uint64_t skv_num_chunks(const skv_params* p);
+uint64_t skv_num_lanes(const skv_params* p);     /* lane_offsets has n_lanes + 1   */
+uint64_t skv_tables_bytes(const skv_params* p);  /* num_tables * SKV_TABLE_STRIDE  */
+uint64_t skv_max_bitstream_bytes(const skv_params* p); /* worst case of any input  */
+uint64_t skv_encode_workspace_bytes(const skv_params* p);
+
+/* Calibration ([SKV] which predictor: residual statistics measured once on a
+ * small calibration set, then frozen; [DCKV] how it differs: a per-component
+ * Laplace).  KV: for every channel, S = sum of |ord(target) - ord(pred)| over
+ * tokens [0, min(n_calib, n_tokens)); the Laplace scale estimate S/N (Q16,
+ * floored) selects one of 32 scale bins (4 per octave over [1/8, 32), clamped).
+ * Writes d_bins[n_channels].  d_sum_abs[n_channels] (u32 S) and
+ * d_hist[n_channels][256] (u32 symbol counts of the calibration tokens) are
+ * optional (NULL to skip); d_hist is accumulated, so the caller zeroes it.
+ * COEF: d_target is ignored (may be NULL), d_pred is beta[n_coef] fp32
+ * (scale / step); bins are 0xFF for beta < 0.05 (switched off, [DCKV] how it
+ * works) or one of 64 bins (8 per octave); d_sum_abs and d_hist must be NULL. */
+int skv_calibrate(const skv_params* p, const void* d_target, const void* d_pred,
+                  uint8_t* d_bins, uint32_t* d_sum_abs, uint32_t* d_hist, void* stream);
+
+/* Builds every probability table of the stream into d_tables
+ * (skv_tables_bytes(p) bytes): Laplace masses integrated over integer cells
+ * ([DCKV] how it differs) from exact integer arithmetic, quantised to
+ * frequencies summing to 4096 with a floor of 1.  Depends only on p's dtype. */
+int skv_build_tables(const skv_params* p, void* d_tables, uint64_t tables_bytes, void* stream);
+
+/* Encode ([SKV] core idea, steps 1-2).  Inputs: d_target and d_pred caches
+ * (COEF: d_target = q int16, d_pred = mu fp32), tables from skv_build_tables
+ * and bins from skv_calibrate.  Outputs: d_bitstream (cap_bytes available)
+ * and d_lane_offsets[n_lanes + 1] (u64 byte offsets).  d_workspace must hold
+ * skv_encode_workspace_bytes(p) bytes.  d_status (one u32) is cleared and then
+ * collects kernel flags.  If h_total_bytes is non-NULL the call synchronises
+ * the stream once, stores the stream size there and returns SKV_ERR_CAPACITY
+ * if it exceeds cap_bytes (the bitstream is then not written); if NULL the call
+ * is fully asynchronous and an overflow sets SKV_FLAG_CAPACITY. */
+int skv_encode(const skv_params* p, const void* d_target, const void* d_pred,
+               const void* d_tables, const uint8_t* d_bins, void* d_bitstream,
+               uint64_t cap_bytes, uint64_t* d_lane_offsets, void* d_workspace,
+               uint64_t workspace_bytes, uint32_t* d_status, uint64_t* h_total_bytes,
+               void* stream);
+
+/* Decode ([SKV] core idea, steps 3-4: the decoder re-uses the same prediction
+ * and adds the decoded residual back).  Writes the exact target bits into
+ * d_target_out (COEF: q int16; switched-off components are 0).  A lane whose
+ * stream does not end in the initial state or does not consume exactly its
+ * words, or offsets that are not increasing and inside n_bytes, set
+ * SKV_FLAG_CORRUPT in d_status (cleared by the call first). */
+int skv_decode(const skv_params* p, const void* d_bitstream, uint64_t n_bytes,
+               const uint64_t* d_lane_offsets, const void* d_pred, const void* d_tables,
+               const uint8_t* d_bins, void* d_target_out, uint32_t* d_status, void* stream);
+
+/* Synchronises the stream, reads the status word and returns SKV_OK or the
+ * code of the most serious flag (CORRUPT > CAPACITY > TIMEOUT > INVALID_ARG
+ * for an out-of-range bin). */
+int skv_read_status(const uint32_t* d_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SKV_H */

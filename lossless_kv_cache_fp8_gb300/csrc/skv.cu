@@ -1,0 +1,1103 @@
+// skv.cu -- speculative KV coding on GB300 (sm_103a): kernels and the C ABI.
+//
+// Hot path: lossless coding of a target KV cache against a predictor's
+// approximation of it ([SKV] "Speculative KV coding", section "core idea"):
+// monotone ordinals, residual symbols with an escape, per-channel Laplace
+// tables from calibration tokens ([SKV] "which predictor"; [DCKV] "how it
+// differs": per-component Laplace integrated over quantisation cells, GPU
+// rANS) and 32-lane interleaved rANS.  Page references:
+//   [SKV]  "Speculative KV coding: losslessly compressing KV cache by up to ~4x"
+//   [DCKV] "DCKV compresses a hybrid language model's prompt KV cache with
+//          learned transform coding"
+//
+// Kernels (all integer; nothing here uses tensor cores because no stage is a
+// dense contraction -- the bound is HBM bandwidth and integer issue):
+//   k_build_tables    one CTA per table: Q32 Taylor exp, power chain, masses,
+//                     largest-remainder frequencies, encoder reciprocals,
+//                     slot->symbol table
+//   k_calibrate_kv    one CTA per (layer, kv, head) slice: exact sum |r| per
+//                     channel over the calibration tokens, warp reductions,
+//                     optional histograms, scale bins
+//   k_encode_kv       persistent warps, one chunk (32 lanes) per warp at a
+//                     time, 128-bit coalesced loads of both caches (each lane
+//                     owns 16-byte groups), encoder tables staged in shared
+//                     memory, reverse pass writing renormalisation words
+//                     downward into the lane's scratch slot
+//   k_scan_*          exclusive scan of lane lengths -> lane byte offsets
+//   k_compact         copies each lane's words from scratch into the stream
+//   k_decode_kv       persistent warps, slot->symbol and decoder tables in
+//                     shared memory, reconstruction fused in: ordinal of the
+//                     prediction + residual, inverse ordinal, 128-bit stores
+//   k_*_coef          the same for transform-coefficient streams (1024 tables
+//                     read through L1/L2; switched-off components skipped)
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "skv.h"
+
+namespace {
+
+constexpr uint32_t kLanes = 32;
+constexpr uint32_t kChain = 2056;        // tau^0 .. tau^2055 covers |16 s + 8 + 15| <= 2055
+constexpr uint32_t kStateLow = 1u << 16; // rANS state lower bound L
+constexpr uint32_t kKvTables = 32;
+constexpr uint32_t kCoefTables = 1024;
+// shared-memory strides per table, padded so that the same symbol of two
+// tables falls in different banks
+constexpr uint32_t kEncSmemStride = 4096 + 16;
+constexpr uint32_t kDecSmemStride = 4096 + 1024 + 4;
+constexpr uint32_t kEncSmemBytes = kKvTables * kEncSmemStride;
+constexpr uint32_t kDecSmemBytes = kKvTables * kDecSmemStride;
+constexpr int kCodecThreads = 1024;
+constexpr int kScanPerBlock = 4096;       // lanes per scan block (256 threads x 16)
+
+// ---------------------------------------------------------------------------
+// Host-side geometry
+// ---------------------------------------------------------------------------
+struct Geo {
+  uint32_t dtype, esz, group, raw_bytes, K, D, C, n_tables, sub;
+  uint64_t T, n_slices, slice_pos, cps, n_chunks, n_lanes, n_channels, n_positions;
+  uint64_t slot_words;
+};
+
+int make_geo(const skv_params* p, Geo* g) {
+  if (!p || !g) return SKV_ERR_INVALID_ARG;
+  if (p->version != SKV_PARAMS_VERSION || p->reserved != 0) return SKV_ERR_INVALID_ARG;
+  memset(g, 0, sizeof(*g));
+  g->dtype = p->dtype;
+  if (p->dtype == SKV_FP8_E4M3) { g->esz = 1; g->group = 16; g->raw_bytes = 1; }
+  else if (p->dtype == SKV_BF16) { g->esz = 2; g->group = 8; g->raw_bytes = 2; }
+  else if (p->dtype == SKV_COEF_I16) { g->esz = 2; g->group = 8; g->raw_bytes = 2; }
+  else return SKV_ERR_INVALID_ARG;
+  g->K = p->lane_syms;
+  if (g->K == 0 || g->K > 65536 || (g->K % g->group) != 0) return SKV_ERR_INVALID_ARG;
+  g->T = p->n_tokens;
+  if (g->T > (1ull << 40)) return SKV_ERR_UNSUPPORTED;
+  if (p->dtype == SKV_COEF_I16) {
+    if (p->n_coef == 0) return SKV_ERR_INVALID_ARG;
+    g->C = p->n_coef;
+    g->n_slices = 1;
+    g->slice_pos = g->T * g->C;
+    g->n_channels = g->C;
+    g->n_tables = kCoefTables;
+    g->sub = 8;
+  } else {
+    g->D = p->head_dim;
+    if (g->D == 0 || (g->D % g->group) != 0 || ((32u * g->group) % g->D) != 0)
+      return SKV_ERR_UNSUPPORTED;
+    if (p->n_calib > 65536) return SKV_ERR_INVALID_ARG;
+    g->n_slices = (uint64_t)p->n_layers * p->n_kv * p->n_heads;
+    g->slice_pos = g->T * g->D;
+    g->n_channels = g->n_slices * g->D;
+    g->n_tables = kKvTables;
+    g->sub = 4;
+  }
+  const uint64_t cs = (uint64_t)kLanes * g->K;
+  g->cps = (g->slice_pos + cs - 1) / cs;
+  g->n_chunks = g->n_slices * g->cps;
+  g->n_lanes = g->n_chunks * kLanes;
+  g->n_positions = g->n_slices * g->slice_pos;
+  if (g->n_positions > (1ull << 44)) return SKV_ERR_UNSUPPORTED;
+  // worst case per lane: 2 state words + one word per coding step, and an
+  // escaped position takes 1 + raw_bytes steps; rounded to 16 bytes
+  g->slot_words = ((2 + (uint64_t)g->K * (1 + g->raw_bytes)) + 7) & ~7ull;
+  return SKV_OK;
+}
+
+uint64_t align256(uint64_t v) { return (v + 255) & ~255ull; }
+
+struct WsLayout {
+  uint64_t slots_off, lw_off, part_off, total;
+  uint64_t n_scan_blocks;
+};
+
+WsLayout ws_layout(const Geo& g) {
+  WsLayout w;
+  w.n_scan_blocks = (g.n_lanes + kScanPerBlock - 1) / kScanPerBlock;
+  w.slots_off = 0;
+  w.lw_off = align256(g.n_lanes * g.slot_words * 2);
+  w.part_off = w.lw_off + align256(g.n_lanes * 4);
+  w.total = w.part_off + align256((w.n_scan_blocks + 1) * 8);
+  return w;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+
+// ordinals of four FP8 patterns at once: non-negative b -> b | 0x80, negative
+// b -> ~b; the inverse flips with the complementary mask
+__device__ __forceinline__ uint32_t ord8x4(uint32_t w) {
+  return w ^ (((w >> 7) & 0x01010101u) * 0x7Fu | 0x80808080u);
+}
+__device__ __forceinline__ uint32_t unord8x4(uint32_t u) {
+  return u ^ (((~u >> 7) & 0x01010101u) * 0x7Fu | 0x80808080u);
+}
+__device__ __forceinline__ uint32_t ord16x2(uint32_t w) {
+  return w ^ (((w >> 15) & 0x00010001u) * 0x7FFFu | 0x80008000u);
+}
+__device__ __forceinline__ uint32_t unord16x2(uint32_t u) {
+  return u ^ (((~u >> 15) & 0x00010001u) * 0x7FFFu | 0x80008000u);
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const void* ptr) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr));
+  return v;
+}
+__device__ __forceinline__ void stg_stream(void* ptr, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(ptr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int k) {
+  return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
+}
+
+// scale bin of q = floor(beta * 2^16): 0 below 1/8, last bin from 32 up,
+// otherwise octave * sub + linear sub-bin below the leading one
+__device__ __forceinline__ uint32_t bin_from_q(uint64_t q, uint32_t sub) {
+  const uint32_t sb = sub == 8 ? 3 : 2;
+  if (q < (1ull << 13)) return 0;
+  if (q >= (1ull << 21)) return 8 * sub - 1;
+  const uint32_t pw = 63 - __clzll((long long)q);
+  return sub * (pw - 13) + (uint32_t)((q >> (pw - sb)) & (sub - 1));
+}
+
+// encoder step with table entry {m_lo, m_hi, fr << 20, (4096 - fr) | cum << 16}
+__device__ __forceinline__ void enc_step(uint32_t& x, uint16_t*& wp, const uint4 e) {
+  if (x >= e.z) {
+    *--wp = (uint16_t)x;
+    x >>= 16;
+  }
+  const uint32_t q = (__umulhi(x, e.x) + x * e.y) >> 12;   // floor(x / fr)
+  x = x + q * (e.w & 0xFFFFu) + (e.w >> 16);
+}
+// raw byte v as a uniform step: fr 16, cum 16 v
+__device__ __forceinline__ void enc_raw(uint32_t& x, uint16_t*& wp, uint32_t v) {
+  if (x >= (1u << 24)) {
+    *--wp = (uint16_t)x;
+    x >>= 16;
+  }
+  x = ((x >> 4) << 12) | (x & 15u) | (v << 4);
+}
+
+struct DecLane {
+  const uint16_t* w;
+  uint32_t n, p, nxt, x;
+};
+__device__ __forceinline__ void dec_renorm(DecLane& L) {
+  if (L.x < kStateLow) {
+    L.x = (L.x << 16) | L.nxt;
+    ++L.p;
+    L.nxt = L.p < L.n ? L.w[L.p] : 0u;
+  }
+}
+__device__ __forceinline__ uint32_t dec_raw(DecLane& L) {
+  const uint32_t slot = L.x & 4095u;
+  L.x = 16u * (L.x >> 12) + (slot & 15u);
+  dec_renorm(L);
+  return slot >> 4;
+}
+__device__ __forceinline__ void dec_open(DecLane& L, const uint8_t* bs, uint64_t a, uint64_t b, bool ok,
+                                         uint32_t* status) {
+  if (!ok) {
+    atomicOr(status, SKV_FLAG_CORRUPT);
+    L.w = nullptr; L.n = 0; L.p = 2; L.nxt = 0; L.x = kStateLow;
+    return;
+  }
+  L.w = reinterpret_cast<const uint16_t*>(bs + a);
+  L.n = (uint32_t)((b - a) >> 1);
+  L.x = ((uint32_t)L.w[0] << 16) | L.w[1];
+  L.p = 2;
+  L.nxt = L.p < L.n ? L.w[L.p] : 0u;
+  if (L.x < kStateLow) atomicOr(status, SKV_FLAG_CORRUPT);
+}
+__device__ __forceinline__ void dec_close(const DecLane& L, uint32_t* status) {
+  if (L.x != kStateLow || L.p != L.n) atomicOr(status, SKV_FLAG_CORRUPT);
+}
+
+// lane offsets [a, b) of lane g, checked against the stream
+__device__ __forceinline__ bool lane_span(const uint64_t* offs, uint64_t g, uint64_t n_lanes,
+                                          uint64_t n_bytes, uint64_t* a, uint64_t* b) {
+  *a = offs[g];
+  *b = offs[g + 1];
+  bool ok = *a <= *b && *b <= n_bytes && ((*a | *b) & 1) == 0 && *b - *a >= 4;
+  if (g == 0 && *a != 0) ok = false;
+  if (g + 1 == n_lanes && *b != n_bytes) ok = false;
+  return ok;
+}
+
+// ---------------------------------------------------------------------------
+// Table builder ([DCKV] how it differs: per-component Laplace integrated over
+// the quantisation cells).  All integer, reproducible on any machine.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_build_tables(uint8_t* blob, uint32_t sub, int coef) {
+  const uint32_t t = blockIdx.x, i = threadIdx.x;
+  const uint32_t bin = coef ? t / 16 : t, f = coef ? t % 16 : 0;
+  __shared__ unsigned long long P[kChain];
+  __shared__ uint32_t rem[256];
+  __shared__ uint32_t cums[257];
+  __shared__ uint32_t red[8];
+  if (i == 0) {
+    // representative scale: midpoint of the sub-bin, Q16
+    const uint32_t e = bin / sub, j = bin % sub;
+    const uint64_t bq = ((1ull << (e + 13)) / (2ull * sub)) * (2ull * sub + 2ull * j + 1ull);
+    const uint64_t xq = ((1ull << 44) + (bq >> 1)) / bq;  // Q32 of 1/(16 beta)
+    uint64_t a = 1ull << 32;
+    long long tau = (long long)a;
+    for (uint64_t n = 1; n <= 15; ++n) {                  // exp(-x) by Taylor
+      a = (a * xq + n * (1ull << 31)) / (n << 32);
+      tau += (n & 1) ? -(long long)a : (long long)a;
+    }
+    const uint64_t tq = (uint64_t)tau;
+    P[0] = 1ull << 32;
+    for (uint32_t n = 1; n < kChain; ++n) P[n] = (P[n - 1] * tq + (1ull << 31)) >> 32;
+  }
+  __syncthreads();
+  auto F = [&](long long n) -> uint64_t {   // Laplace CDF at n/16 from the mean, Q32
+    return n < 0 ? (P[-n] >> 1) : ((1ull << 32) - (P[n] >> 1));
+  };
+  uint64_t m;
+  if (i < 255) {
+    const long long s = (long long)i - 127;
+    m = F(16 * s + 8 - (long long)f) - F(16 * s - 8 - (long long)f);
+  } else {
+    m = F(-16 * 127 - 8 - (long long)f) + ((1ull << 32) - F(16 * 127 + 8 - (long long)f));
+  }
+  const uint64_t scaled = m * 3840ull;
+  uint32_t fr = 1u + (uint32_t)(scaled >> 32);
+  const uint32_t rm = (uint32_t)scaled;
+  rem[i] = rm;
+  // block sum of the floors
+  uint32_t s = fr;
+  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+  if ((i & 31) == 0) red[i >> 5] = s;
+  __syncthreads();
+  uint32_t total = 0;
+  for (int k = 0; k < 8; ++k) total += red[k];
+  const uint32_t deficit = 4096u - total;
+  // largest remainders get one more unit; ties go to the lower symbol
+  uint32_t rank = 0;
+  for (uint32_t k = 0; k < 256; ++k) {
+    const uint32_t r2 = rem[k];
+    rank += (r2 > rm) || (r2 == rm && k < i);
+  }
+  fr += rank < deficit ? 1u : 0u;
+  // exclusive scan of fr
+  uint32_t incl = fr;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if ((i & 31) >= (uint32_t)o) incl += v;
+  }
+  __syncthreads();
+  if ((i & 31) == 31) red[i >> 5] = incl;
+  __syncthreads();
+  uint32_t base = 0;
+  for (uint32_t k = 0; k < (i >> 5); ++k) base += red[k];
+  const uint32_t cum = base + incl - fr;
+  cums[i] = cum;
+  if (i == 255) cums[256] = 4096;
+  uint8_t* tb = blob + (uint64_t)t * SKV_TABLE_STRIDE;
+  reinterpret_cast<uint16_t*>(tb + SKV_TABLE_FREQ_OFF)[i] = (uint16_t)fr;
+  reinterpret_cast<uint16_t*>(tb + SKV_TABLE_CUM_OFF)[i] = (uint16_t)cum;
+  if (i == 255) reinterpret_cast<uint16_t*>(tb + SKV_TABLE_CUM_OFF)[256] = 4096;
+  const uint64_t mm = ((1ull << 44) + fr - 1) / fr;   // ceil(2^44 / fr)
+  uint4 enc;
+  enc.x = (uint32_t)mm;
+  enc.y = (uint32_t)(mm >> 32);
+  enc.z = fr << 20;
+  enc.w = (4096u - fr) | (cum << 16);
+  reinterpret_cast<uint4*>(tb + SKV_TABLE_ENC_OFF)[i] = enc;
+  reinterpret_cast<uint32_t*>(tb + SKV_TABLE_DEC_OFF)[i] = fr | (cum << 16);
+  __syncthreads();
+  // slot -> symbol: the last symbol whose cum <= slot
+  uint8_t* lut = tb + SKV_TABLE_LUT_OFF;
+  for (uint32_t k = 0; k < 16; ++k) {
+    const uint32_t slot = i * 16 + k;
+    uint32_t lo = 0, hi = 256;
+    while (hi - lo > 1) {
+      const uint32_t mid = (lo + hi) >> 1;
+      if (cums[mid] <= slot) lo = mid; else hi = mid;
+    }
+    lut[slot] = (uint8_t)lo;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Calibration ([SKV] which predictor: statistics measured once on calibration
+// tokens and frozen).  One CTA per slice, each thread covers 16-byte groups of
+// channels for a stride of tokens; partial sums are combined across the lanes
+// that share a channel group with warp shuffles, then across warps.
+// ---------------------------------------------------------------------------
+template <int ESZ>
+__global__ void __launch_bounds__(256) k_calibrate_kv(const uint8_t* tgt, const uint8_t* prd,
+                                                      uint8_t* bins, uint32_t* sum_abs,
+                                                      uint32_t* hist, uint64_t T, uint32_t D,
+                                                      uint32_t nc) {
+  constexpr int G = 16 / ESZ;
+  __shared__ unsigned long long S[512];
+  const uint64_t slice = blockIdx.x;
+  const uint32_t nv = D / G;                    // 16-byte groups per token (<= 32)
+  const uint32_t tid = threadIdx.x;
+  const uint32_t cg = tid % nv, tph = tid / nv, nph = blockDim.x / nv;
+  for (uint32_t d = tid; d < D; d += blockDim.x) S[d] = 0;
+  __syncthreads();
+  uint32_t acc[G];
+#pragma unroll
+  for (int e = 0; e < G; ++e) acc[e] = 0;
+  const uint64_t base = slice * T * D;          // element index of the slice
+  if (tph < nph) {
+    for (uint64_t t = tph; t < nc; t += nph) {
+      const uint64_t el = base + t * D + (uint64_t)cg * G;
+      const uint4 tv = ldg_stream(tgt + el * ESZ), pv = ldg_stream(prd + el * ESZ);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t a = ESZ == 1 ? ord8x4(word_of(tv, k)) : ord16x2(word_of(tv, k));
+        const uint32_t b = ESZ == 1 ? ord8x4(word_of(pv, k)) : ord16x2(word_of(pv, k));
+#pragma unroll
+        for (int h = 0; h < 4 / ESZ; ++h) {
+          const uint32_t sh = 8 * ESZ * h, mk = ESZ == 1 ? 0xFFu : 0xFFFFu;
+          const int r = (int)((a >> sh) & mk) - (int)((b >> sh) & mk);
+          const int e = k * (4 / ESZ) + h;
+          acc[e] += (uint32_t)(r < 0 ? -r : r);
+          if (hist) {
+            const uint32_t sym = (r >= -127 && r <= 127) ? (uint32_t)(r + 127) : 255u;
+            atomicAdd(&hist[((slice * D) + (uint64_t)cg * G + e) * 256 + sym], 1u);
+          }
+        }
+      }
+    }
+  }
+  // lanes tid, tid + nv, ... of one warp share a channel group
+#pragma unroll
+  for (int e = 0; e < G; ++e) {
+    uint32_t v = acc[e];
+    for (uint32_t o = nv; o < 32; o <<= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    acc[e] = v;
+  }
+  if ((tid & 31) < nv && tph < nph) {
+#pragma unroll
+    for (int e = 0; e < G; ++e) atomicAdd(&S[cg * G + e], (unsigned long long)acc[e]);
+  }
+  __syncthreads();
+  for (uint32_t d = tid; d < D; d += blockDim.x) {
+    const uint64_t sv = S[d];
+    const uint64_t q = nc ? (sv << 16) / nc : 0;
+    bins[slice * D + d] = (uint8_t)bin_from_q(q, 4);
+    if (sum_abs) sum_abs[slice * D + d] = (uint32_t)sv;
+  }
+}
+
+// COEF: bins from beta = scale/step; below 0.05 the component is switched off
+// ([DCKV] how it works)
+__global__ void k_calibrate_coef(const float* beta, uint8_t* bins, uint32_t C) {
+  const uint32_t c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= C) return;
+  const float b = beta[c];
+  uint8_t out;
+  if (!(b >= 0.05f)) out = 0xFF;
+  else if (b >= 32.0f) out = 63;
+  else out = (uint8_t)bin_from_q((uint64_t)floorf(__fmul_rn(b, 65536.0f)), 8);
+  bins[c] = out;
+}
+
+// ---------------------------------------------------------------------------
+// Encoder, KV caches.  Persistent warps; warp w takes chunks w, w + W, ...
+// Lane l of a chunk owns 16-byte groups l, l + 32, ...; the reverse pass walks
+// them from the last group down, prefetching the next group's 128-bit loads.
+// ---------------------------------------------------------------------------
+struct CodecArgs {
+  const uint8_t* tgt;   // encode: target; decode: unused
+  const uint8_t* prd;   // prediction (COEF: mu)
+  uint8_t* out;         // decode: target output
+  const uint8_t* tables;
+  const uint8_t* bins;
+  uint16_t* slots;      // encode scratch
+  uint32_t* lane_words;
+  const uint8_t* bs;    // decode: bitstream
+  const uint64_t* offs; // decode: lane offsets
+  uint64_t n_bytes;
+  uint32_t* status;
+  uint64_t n_chunks, cps, slice_pos, n_lanes, slot_words;
+  uint32_t K, D, C;
+};
+
+template <int ESZ>
+__device__ __forceinline__ void load_lane_tables(const CodecArgs& a, uint64_t slice, uint32_t d0,
+                                                 uint32_t stride, uint32_t* tb) {
+  constexpr int G = 16 / ESZ;
+  const uint8_t* bp = a.bins + slice * a.D + d0;
+  uint32_t bw[4];
+  if (G == 16) {
+    const uint4 v = *reinterpret_cast<const uint4*>(bp);
+    bw[0] = v.x; bw[1] = v.y; bw[2] = v.z; bw[3] = v.w;
+  } else {
+    const uint2 v = *reinterpret_cast<const uint2*>(bp);
+    bw[0] = v.x; bw[1] = v.y; bw[2] = 0; bw[3] = 0;
+  }
+  bool bad = false;
+#pragma unroll
+  for (int e = 0; e < G; ++e) {
+    uint32_t b = (bw[e >> 2] >> (8 * (e & 3))) & 0xFFu;
+    if (b >= kKvTables) { bad = true; b = kKvTables - 1; }
+    tb[e] = b * stride;
+  }
+  if (bad) atomicOr(a.status, SKV_FLAG_BAD_BIN);
+}
+
+template <int ESZ>
+__global__ void __launch_bounds__(kCodecThreads, 1) k_encode_kv(CodecArgs a) {
+  constexpr int G = 16 / ESZ;
+  extern __shared__ __align__(16) uint8_t smem[];
+  // stage the 32 encoder tables
+  for (uint32_t k = threadIdx.x; k < kKvTables * 256; k += blockDim.x) {
+    const uint32_t t = k >> 8, s = k & 255;
+    *reinterpret_cast<uint4*>(smem + t * kEncSmemStride + s * 16) =
+        reinterpret_cast<const uint4*>(a.tables + (uint64_t)t * SKV_TABLE_STRIDE + SKV_TABLE_ENC_OFF)[s];
+  }
+  __syncthreads();
+  const uint32_t lane = threadIdx.x & 31;
+  const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
+  const uint64_t chunk_pos = (uint64_t)kLanes * a.K;
+  for (uint64_t chunk = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); chunk < a.n_chunks;
+       chunk += warps) {
+    const uint64_t slice = chunk / a.cps;
+    const uint64_t first = (chunk - slice * a.cps) * chunk_pos;
+    const uint64_t n_pos = min(chunk_pos, a.slice_pos - first);
+    const uint32_t n_groups = (uint32_t)(n_pos / G);
+    const uint32_t n_g = lane < n_groups ? (n_groups - lane + 31) / 32 : 0;
+    uint32_t tb[G];
+    load_lane_tables<ESZ>(a, slice, (lane * G) % a.D, kEncSmemStride, tb);
+    const uint8_t* tg = a.tgt + (slice * a.slice_pos + first) * ESZ + lane * 16;
+    const uint8_t* pd = a.prd + (slice * a.slice_pos + first) * ESZ + lane * 16;
+    const uint64_t g = chunk * kLanes + lane;
+    uint16_t* const slot_end = a.slots + (g + 1) * a.slot_words;
+    uint16_t* wp = slot_end;
+    uint32_t x = kStateLow;
+    uint4 tc = make_uint4(0, 0, 0, 0), pc = tc;
+    if (n_g) {
+      tc = ldg_stream(tg + (uint64_t)(n_g - 1) * 512);
+      pc = ldg_stream(pd + (uint64_t)(n_g - 1) * 512);
+    }
+    for (int i = (int)n_g - 1; i >= 0; --i) {
+      uint4 tn = tc, pn = pc;
+      if (i > 0) {
+        tn = ldg_stream(tg + (uint64_t)(i - 1) * 512);
+        pn = ldg_stream(pd + (uint64_t)(i - 1) * 512);
+      }
+      uint32_t tw[4], pw[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        tw[k] = ESZ == 1 ? ord8x4(word_of(tc, k)) : ord16x2(word_of(tc, k));
+        pw[k] = ESZ == 1 ? ord8x4(word_of(pc, k)) : ord16x2(word_of(pc, k));
+      }
+#pragma unroll
+      for (int e = G - 1; e >= 0; --e) {
+        constexpr uint32_t mk = ESZ == 1 ? 0xFFu : 0xFFFFu;
+        const uint32_t sh = ESZ == 1 ? 8 * (e & 3) : 16 * (e & 1);
+        const int wi = ESZ == 1 ? (e >> 2) : (e >> 1);
+        const int r = (int)((tw[wi] >> sh) & mk) - (int)((pw[wi] >> sh) & mk);
+        uint32_t sym = (uint32_t)(r + 127);
+        if (sym > 254u) {
+          const uint32_t raw = (uint32_t)r & mk;
+          enc_raw(x, wp, raw & 0xFFu);
+          if (ESZ == 2) enc_raw(x, wp, raw >> 8);
+          sym = 255;
+        }
+        const uint4 en = *reinterpret_cast<const uint4*>(smem + tb[e] + sym * 16);
+        enc_step(x, wp, en);
+      }
+      tc = tn;
+      pc = pn;
+    }
+    *--wp = (uint16_t)x;
+    *--wp = (uint16_t)(x >> 16);
+    a.lane_words[g] = (uint32_t)(slot_end - wp);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Decoder, KV caches, fused with reconstruction.
+// ---------------------------------------------------------------------------
+template <int ESZ>
+__global__ void __launch_bounds__(kCodecThreads, 1) k_decode_kv(CodecArgs a) {
+  constexpr int G = 16 / ESZ;
+  extern __shared__ __align__(16) uint8_t smem[];
+  // stage LUT (4096 B) + decoder entries (1024 B) of the 32 tables
+  for (uint32_t k = threadIdx.x; k < kKvTables * 320; k += blockDim.x) {
+    const uint32_t t = k / 320, s = k % 320;
+    const uint4 v = reinterpret_cast<const uint4*>(a.tables + (uint64_t)t * SKV_TABLE_STRIDE +
+                                                   SKV_TABLE_LUT_OFF)[s];
+    uint32_t* dst = reinterpret_cast<uint32_t*>(smem + t * kDecSmemStride + s * 16);
+    dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
+  }
+  __syncthreads();
+  const uint32_t lane = threadIdx.x & 31;
+  const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
+  const uint64_t chunk_pos = (uint64_t)kLanes * a.K;
+  for (uint64_t chunk = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); chunk < a.n_chunks;
+       chunk += warps) {
+    const uint64_t slice = chunk / a.cps;
+    const uint64_t first = (chunk - slice * a.cps) * chunk_pos;
+    const uint64_t n_pos = min(chunk_pos, a.slice_pos - first);
+    const uint32_t n_groups = (uint32_t)(n_pos / G);
+    const uint32_t n_g = lane < n_groups ? (n_groups - lane + 31) / 32 : 0;
+    uint32_t tb[G];
+    load_lane_tables<ESZ>(a, slice, (lane * G) % a.D, kDecSmemStride, tb);
+    const uint64_t g = chunk * kLanes + lane;
+    uint64_t sa, sb;
+    const bool ok = lane_span(a.offs, g, a.n_lanes, a.n_bytes, &sa, &sb);
+    DecLane L;
+    dec_open(L, a.bs, sa, sb, ok, a.status);
+    const uint8_t* pd = a.prd + (slice * a.slice_pos + first) * ESZ + lane * 16;
+    uint8_t* od = a.out + (slice * a.slice_pos + first) * ESZ + lane * 16;
+    uint4 pc = make_uint4(0, 0, 0, 0);
+    if (n_g) pc = ldg_stream(pd);
+    for (uint32_t i = 0; i < n_g; ++i) {
+      uint4 pn = pc;
+      if (i + 1 < n_g) pn = ldg_stream(pd + (uint64_t)(i + 1) * 512);
+      uint32_t pw[4], ow[4] = {0, 0, 0, 0};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) pw[k] = ESZ == 1 ? ord8x4(word_of(pc, k)) : ord16x2(word_of(pc, k));
+#pragma unroll
+      for (int e = 0; e < G; ++e) {
+        constexpr uint32_t mk = ESZ == 1 ? 0xFFu : 0xFFFFu;
+        const uint32_t sh = ESZ == 1 ? 8 * (e & 3) : 16 * (e & 1);
+        const int wi = ESZ == 1 ? (e >> 2) : (e >> 1);
+        const uint32_t slot = L.x & 4095u;
+        const uint32_t sym = smem[tb[e] + slot];
+        const uint32_t dv = *reinterpret_cast<const uint32_t*>(smem + tb[e] + 4096 + sym * 4);
+        L.x = (dv & 0xFFFFu) * (L.x >> 12) + slot - (dv >> 16);
+        dec_renorm(L);
+        uint32_t r;
+        if (sym == 255u) {
+          r = dec_raw(L);
+          if (ESZ == 2) r = (r << 8) | dec_raw(L);
+        } else {
+          r = sym - 127u;
+        }
+        const uint32_t ut = (((pw[wi] >> sh) & mk) + r) & mk;
+        ow[wi] |= ut << sh;
+      }
+      uint4 o;
+      o.x = ESZ == 1 ? unord8x4(ow[0]) : unord16x2(ow[0]);
+      o.y = ESZ == 1 ? unord8x4(ow[1]) : unord16x2(ow[1]);
+      o.z = ESZ == 1 ? unord8x4(ow[2]) : unord16x2(ow[2]);
+      o.w = ESZ == 1 ? unord8x4(ow[3]) : unord16x2(ow[3]);
+      stg_stream(od + (uint64_t)i * 512, o);
+      pc = pn;
+    }
+    dec_close(L, a.status);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Transform-coefficient streams (int16 q, fp32 mean mu, 1024 tables).
+// Positions are the full [token][coef] grid; switched-off components carry
+// no symbol.  Tables are read through the cache hierarchy.
+// ---------------------------------------------------------------------------
+// mu -> (m, f): mu rounded to the nearest 1/16 (ties up) in fp32,
+// m = floor(mu_q / 16), f = mu_q mod 16
+__device__ __forceinline__ void coef_mean(float mu, int* m, uint32_t* f) {
+  const float t = __fadd_rn(__fmul_rn(mu, 16.0f), 0.5f);
+  const int mq = fabsf(t) < 67108864.0f ? (int)floorf(t) : 0;
+  *m = mq >> 4;
+  *f = (uint32_t)mq & 15u;
+}
+
+__global__ void __launch_bounds__(256) k_encode_coef(CodecArgs a) {
+  const uint32_t lane = threadIdx.x & 31;
+  const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
+  const uint64_t chunk_pos = (uint64_t)kLanes * a.K;
+  const int16_t* q = reinterpret_cast<const int16_t*>(a.tgt);
+  const float* mu = reinterpret_cast<const float*>(a.prd);
+  for (uint64_t chunk = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); chunk < a.n_chunks;
+       chunk += warps) {
+    const uint64_t first = chunk * chunk_pos;
+    const uint64_t n_pos = min(chunk_pos, a.slice_pos - first);
+    const uint32_t n_groups = (uint32_t)((n_pos + 7) / 8);
+    const uint32_t n_g = lane < n_groups ? (n_groups - lane + 31) / 32 : 0;
+    const uint64_t g = chunk * kLanes + lane;
+    uint16_t* const slot_end = a.slots + (g + 1) * a.slot_words;
+    uint16_t* wp = slot_end;
+    uint32_t x = kStateLow;
+    for (int i = (int)n_g - 1; i >= 0; --i) {
+      const uint64_t p0 = first + ((uint64_t)i * 32 + lane) * 8;   // position of the group
+      const uint32_t ne = (uint32_t)min((uint64_t)8, first + n_pos - p0);
+      uint32_t c = (uint32_t)((p0 + ne - 1) % a.C);                 // component of the last element
+      for (int e = (int)ne - 1; e >= 0; --e) {
+        const uint32_t bin = a.bins[c];
+        const uint64_t pos = p0 + (uint32_t)e;
+        c = c == 0 ? a.C - 1 : c - 1;
+        if (bin == 0xFFu) continue;
+        int m;
+        uint32_t f;
+        coef_mean(__ldg(mu + pos), &m, &f);
+        const int r = (int)__ldg(q + pos) - m;
+        uint32_t sym = (uint32_t)(r + 127);
+        if (sym > 254u) {
+          const uint32_t raw = (uint32_t)r & 0xFFFFu;
+          enc_raw(x, wp, raw & 0xFFu);
+          enc_raw(x, wp, raw >> 8);
+          sym = 255;
+        }
+        uint32_t tbl = 16u * bin + f;
+        if (bin > 63u) { atomicOr(a.status, SKV_FLAG_BAD_BIN); tbl = 1023; }
+        const uint4 en = __ldg(reinterpret_cast<const uint4*>(a.tables + (uint64_t)tbl * SKV_TABLE_STRIDE +
+                                                              SKV_TABLE_ENC_OFF) + sym);
+        enc_step(x, wp, en);
+      }
+    }
+    *--wp = (uint16_t)x;
+    *--wp = (uint16_t)(x >> 16);
+    a.lane_words[g] = (uint32_t)(slot_end - wp);
+  }
+}
+
+__global__ void __launch_bounds__(256) k_decode_coef(CodecArgs a) {
+  const uint32_t lane = threadIdx.x & 31;
+  const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
+  const uint64_t chunk_pos = (uint64_t)kLanes * a.K;
+  int16_t* q = reinterpret_cast<int16_t*>(a.out);
+  const float* mu = reinterpret_cast<const float*>(a.prd);
+  for (uint64_t chunk = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); chunk < a.n_chunks;
+       chunk += warps) {
+    const uint64_t first = chunk * chunk_pos;
+    const uint64_t n_pos = min(chunk_pos, a.slice_pos - first);
+    const uint32_t n_groups = (uint32_t)((n_pos + 7) / 8);
+    const uint32_t n_g = lane < n_groups ? (n_groups - lane + 31) / 32 : 0;
+    const uint64_t g = chunk * kLanes + lane;
+    uint64_t sa, sb;
+    const bool ok = lane_span(a.offs, g, a.n_lanes, a.n_bytes, &sa, &sb);
+    DecLane L;
+    dec_open(L, a.bs, sa, sb, ok, a.status);
+    for (uint32_t i = 0; i < n_g; ++i) {
+      const uint64_t p0 = first + ((uint64_t)i * 32 + lane) * 8;
+      const uint32_t ne = (uint32_t)min((uint64_t)8, first + n_pos - p0);
+      uint32_t c = (uint32_t)(p0 % a.C);
+      for (uint32_t e = 0; e < ne; ++e) {
+        const uint32_t bin = a.bins[c];
+        const uint64_t pos = p0 + e;
+        c = c + 1 == a.C ? 0 : c + 1;
+        if (bin == 0xFFu) { q[pos] = 0; continue; }
+        int m;
+        uint32_t f;
+        coef_mean(__ldg(mu + pos), &m, &f);
+        uint32_t tbl = 16u * bin + f;
+        if (bin > 63u) { atomicOr(a.status, SKV_FLAG_BAD_BIN); tbl = 1023; }
+        const uint8_t* tb = a.tables + (uint64_t)tbl * SKV_TABLE_STRIDE;
+        const uint32_t slot = L.x & 4095u;
+        const uint32_t sym = __ldg(tb + SKV_TABLE_LUT_OFF + slot);
+        const uint32_t dv = __ldg(reinterpret_cast<const uint32_t*>(tb + SKV_TABLE_DEC_OFF) + sym);
+        L.x = (dv & 0xFFFFu) * (L.x >> 12) + slot - (dv >> 16);
+        dec_renorm(L);
+        uint32_t r;
+        if (sym == 255u) {
+          r = dec_raw(L);
+          r = (r << 8) | dec_raw(L);
+        } else {
+          r = (uint32_t)((int)sym - 127);
+        }
+        q[pos] = (int16_t)(uint16_t)(((uint32_t)m + r) & 0xFFFFu);
+      }
+    }
+    dec_close(L, a.status);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Lane lengths -> byte offsets: three-phase exclusive scan, then compaction.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_scan_reduce(const uint32_t* lw, uint64_t n,
+                                                     unsigned long long* part) {
+  __shared__ unsigned long long red[8];
+  const uint64_t b0 = (uint64_t)blockIdx.x * kScanPerBlock;
+  unsigned long long s = 0;
+  for (uint32_t k = threadIdx.x; k < kScanPerBlock; k += 256) {
+    const uint64_t i = b0 + k;
+    if (i < n) s += lw[i];
+  }
+  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long t = 0;
+    for (int k = 0; k < 8; ++k) t += red[k];
+    part[blockIdx.x] = t;
+  }
+}
+
+// exclusive scan of part[0..nb) in place; single CTA of 1024 threads
+__global__ void __launch_bounds__(1024) k_scan_parts(unsigned long long* part, uint64_t nb) {
+  __shared__ unsigned long long wsum[32];
+  __shared__ unsigned long long carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (uint64_t base = 0; base < nb; base += 1024) {
+    const uint64_t i = base + threadIdx.x;
+    const unsigned long long v = i < nb ? part[i] : 0;
+    unsigned long long incl = v;
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if ((threadIdx.x & 31) >= (uint32_t)o) incl += u;
+    }
+    if ((threadIdx.x & 31) == 31) wsum[threadIdx.x >> 5] = incl;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      unsigned long long w = wsum[threadIdx.x], wi = w;
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long u = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+        if (threadIdx.x >= (uint32_t)o) wi += u;
+      }
+      wsum[threadIdx.x] = wi - w;   // exclusive warp offsets
+    }
+    __syncthreads();
+    const unsigned long long excl = carry + wsum[threadIdx.x >> 5] + incl - v;
+    __syncthreads();
+    if (i < nb) part[i] = excl;
+    if (threadIdx.x == 1023) carry = excl + v;
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(256) k_scan_write(const uint32_t* lw, uint64_t n,
+                                                    const unsigned long long* part, uint64_t* offs) {
+  __shared__ unsigned long long wsum[8];
+  const uint64_t b0 = (uint64_t)blockIdx.x * kScanPerBlock;
+  // each thread owns 16 consecutive lanes
+  const uint64_t i0 = b0 + (uint64_t)threadIdx.x * 16;
+  uint32_t v[16];
+  unsigned long long s = 0;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    v[k] = (i0 + k < n) ? lw[i0 + k] : 0u;
+    s += v[k];
+  }
+  unsigned long long incl = s;
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if ((threadIdx.x & 31) >= (uint32_t)o) incl += u;
+  }
+  if ((threadIdx.x & 31) == 31) wsum[threadIdx.x >> 5] = incl;
+  __syncthreads();
+  unsigned long long wbase = 0;
+  for (uint32_t k = 0; k < (threadIdx.x >> 5); ++k) wbase += wsum[k];
+  unsigned long long run = part[blockIdx.x] + wbase + incl - s;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const uint64_t i = i0 + k;
+    if (i < n) {
+      offs[i] = 2ull * run;
+      run += v[k];
+      if (i + 1 == n) offs[n] = 2ull * run;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) k_compact(const uint16_t* slots, const uint32_t* lw,
+                                                 const uint64_t* offs, uint64_t n_lanes,
+                                                 uint64_t slot_words, uint8_t* bs, uint64_t cap,
+                                                 uint32_t* status) {
+  const uint32_t lane = threadIdx.x & 31;
+  const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
+  for (uint64_t g = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); g < n_lanes; g += warps) {
+    const uint32_t n = lw[g];
+    const uint64_t dst = offs[g];
+    if (dst + 2ull * n > cap) {
+      if (lane == 0) atomicOr(status, SKV_FLAG_CAPACITY);
+      continue;
+    }
+    const uint16_t* src = slots + (g + 1) * slot_words - n;
+    uint16_t* d = reinterpret_cast<uint16_t*>(bs + dst);
+    for (uint32_t k = lane; k < n; k += 32) d[k] = src[k];
+  }
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? SKV_OK : SKV_ERR_CUDA; }
+
+int launch_check() { return cuda_status(cudaGetLastError()); }
+
+template <typename Kern>
+int set_smem(Kern k, int bytes) {
+  return cuda_status(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+}
+
+// blocks for a persistent codec kernel: one CTA per SM, warps spread so that
+// every SM gets work when there are few chunks
+void codec_grid(uint64_t n_chunks, int* blocks, int* threads) {
+  int sms = sm_count();
+  if (sms <= 0) sms = 1;
+  uint64_t warps_per_block = (n_chunks + sms - 1) / sms;
+  if (warps_per_block > kCodecThreads / 32) warps_per_block = kCodecThreads / 32;
+  if (warps_per_block < 1) warps_per_block = 1;
+  uint64_t nb = (n_chunks + warps_per_block - 1) / warps_per_block;
+  if (nb > (uint64_t)sms) nb = sms;
+  *blocks = (int)(nb < 1 ? 1 : nb);
+  *threads = (int)(warps_per_block * 32);
+}
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+extern "C" {
+
+const char* skv_status_string(int status) {
+  switch (status) {
+    case SKV_OK: return "ok";
+    case SKV_ERR_INVALID_ARG: return "invalid argument";
+    case SKV_ERR_CUDA: return "CUDA error";
+    case SKV_ERR_CAPACITY: return "output buffer too small";
+    case SKV_ERR_CORRUPT: return "corrupt bitstream";
+    case SKV_ERR_TIMEOUT: return "timeout";
+    case SKV_ERR_UNSUPPORTED: return "unsupported parameters";
+    default: return "unknown status";
+  }
+}
+
+int skv_check_params(const skv_params* p) {
+  Geo g;
+  return make_geo(p, &g);
+}
+
+uint64_t skv_num_positions(const skv_params* p) {
+  Geo g;
+  return make_geo(p, &g) == SKV_OK ? g.n_positions : 0;
+}
+uint64_t skv_num_channels(const skv_params* p) {
+  Geo g;
+  return make_geo(p, &g) == SKV_OK ? g.n_channels : 0;
+}
+uint32_t skv_num_tables(const skv_params* p) {
+  Geo g;
+  return make_geo(p, &g) == SKV_OK ? g.n_tables : 0;
+}
+uint64_t skv_num_chunks(const skv_params* p) {
+  Geo g;
+  return make_geo(p, &g) == SKV_OK ? g.n_chunks : 0;
+}
+uint64_t skv_num_lanes(const skv_params* p) {
+  Geo g;
+  return make_geo(p, &g) == SKV_OK ? g.n_lanes : 0;
+}
+uint64_t skv_tables_bytes(const skv_params* p) {
+  Geo g;
+  return make_geo(p, &g) == SKV_OK ? (uint64_t)g.n_tables * SKV_TABLE_STRIDE : 0;
+}
+uint64_t skv_max_bitstream_bytes(const skv_params* p) {
+  Geo g;
+  if (make_geo(p, &g) != SKV_OK) return 0;
+  return 4ull * g.n_lanes + 2ull * (1 + g.raw_bytes) * g.n_positions;
+}
+uint64_t skv_encode_workspace_bytes(const skv_params* p) {
+  Geo g;
+  if (make_geo(p, &g) != SKV_OK) return 0;
+  return ws_layout(g).total;
+}
+
+int skv_calibrate(const skv_params* p, const void* d_target, const void* d_pred, uint8_t* d_bins,
+                  uint32_t* d_sum_abs, uint32_t* d_hist, void* stream) {
+  Geo g;
+  int st = make_geo(p, &g);
+  if (st != SKV_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (g.n_channels == 0) return SKV_OK;
+  if (!d_pred || !d_bins) return SKV_ERR_INVALID_ARG;
+  if (g.dtype == SKV_COEF_I16) {
+    if (d_sum_abs || d_hist) return SKV_ERR_INVALID_ARG;
+    k_calibrate_coef<<<(unsigned)((g.C + 255) / 256), 256, 0, s>>>(static_cast<const float*>(d_pred), d_bins, g.C);
+    return launch_check();
+  }
+  if (!d_target || !aligned16(d_target) || !aligned16(d_pred)) return SKV_ERR_INVALID_ARG;
+  const uint32_t nc = (uint32_t)(p->n_calib < g.T ? p->n_calib : g.T);
+  if (g.n_slices > 0x7FFFFFFFull) return SKV_ERR_UNSUPPORTED;
+  if (g.esz == 1)
+    k_calibrate_kv<1><<<(unsigned)g.n_slices, 256, 0, s>>>(static_cast<const uint8_t*>(d_target),
+                                                            static_cast<const uint8_t*>(d_pred), d_bins,
+                                                            d_sum_abs, d_hist, g.T, g.D, nc);
+  else
+    k_calibrate_kv<2><<<(unsigned)g.n_slices, 256, 0, s>>>(static_cast<const uint8_t*>(d_target),
+                                                            static_cast<const uint8_t*>(d_pred), d_bins,
+                                                            d_sum_abs, d_hist, g.T, g.D, nc);
+  return launch_check();
+}
+
+int skv_build_tables(const skv_params* p, void* d_tables, uint64_t tables_bytes, void* stream) {
+  Geo g;
+  int st = make_geo(p, &g);
+  if (st != SKV_OK) return st;
+  if (!d_tables || !aligned16(d_tables) || tables_bytes < (uint64_t)g.n_tables * SKV_TABLE_STRIDE)
+    return SKV_ERR_INVALID_ARG;
+  k_build_tables<<<g.n_tables, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint8_t*>(d_tables), g.sub, g.dtype == SKV_COEF_I16 ? 1 : 0);
+  return launch_check();
+}
+
+int skv_encode(const skv_params* p, const void* d_target, const void* d_pred, const void* d_tables,
+               const uint8_t* d_bins, void* d_bitstream, uint64_t cap_bytes, uint64_t* d_lane_offsets,
+               void* d_workspace, uint64_t workspace_bytes, uint32_t* d_status, uint64_t* h_total_bytes,
+               void* stream) {
+  Geo g;
+  int st = make_geo(p, &g);
+  if (st != SKV_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!d_status || !d_lane_offsets || ((uintptr_t)d_status & 3) || ((uintptr_t)d_lane_offsets & 7))
+    return SKV_ERR_INVALID_ARG;
+  const WsLayout wl = ws_layout(g);
+  if (g.n_lanes == 0) {
+    st = cuda_status(cudaMemsetAsync(d_status, 0, 4, s));
+    if (st == SKV_OK) st = cuda_status(cudaMemsetAsync(d_lane_offsets, 0, 8, s));
+    if (st == SKV_OK && h_total_bytes) {
+      *h_total_bytes = 0;
+      st = cuda_status(cudaStreamSynchronize(s));
+    }
+    return st;
+  }
+  if (!d_target || !d_pred || !d_tables || !d_bins || !d_bitstream || !d_workspace) return SKV_ERR_INVALID_ARG;
+  if (!aligned16(d_target) || !aligned16(d_pred) || !aligned16(d_tables) || !aligned16(d_bins) ||
+      !aligned16(d_workspace) || ((uintptr_t)d_bitstream & 1))
+    return SKV_ERR_INVALID_ARG;
+  if (workspace_bytes < wl.total) return SKV_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(d_workspace);
+  CodecArgs a;
+  memset(&a, 0, sizeof(a));
+  a.tgt = static_cast<const uint8_t*>(d_target);
+  a.prd = static_cast<const uint8_t*>(d_pred);
+  a.tables = static_cast<const uint8_t*>(d_tables);
+  a.bins = d_bins;
+  a.slots = reinterpret_cast<uint16_t*>(ws + wl.slots_off);
+  a.lane_words = reinterpret_cast<uint32_t*>(ws + wl.lw_off);
+  a.status = d_status;
+  a.n_chunks = g.n_chunks;
+  a.cps = g.cps;
+  a.slice_pos = g.slice_pos;
+  a.n_lanes = g.n_lanes;
+  a.slot_words = g.slot_words;
+  a.K = g.K;
+  a.D = g.D;
+  a.C = g.C;
+  st = cuda_status(cudaMemsetAsync(d_status, 0, 4, s));
+  if (st != SKV_OK) return st;
+  int blocks, threads;
+  if (g.dtype == SKV_COEF_I16) {
+    int sms = sm_count();
+    uint64_t nb = (g.n_chunks + 7) / 8;
+    uint64_t cap_blocks = (uint64_t)(sms > 0 ? sms : 1) * 8;
+    k_encode_coef<<<(unsigned)(nb < cap_blocks ? nb : cap_blocks), 256, 0, s>>>(a);
+  } else {
+    codec_grid(g.n_chunks, &blocks, &threads);
+    if (g.esz == 1) {
+      if ((st = set_smem(k_encode_kv<1>, kEncSmemBytes)) != SKV_OK) return st;
+      k_encode_kv<1><<<blocks, threads, kEncSmemBytes, s>>>(a);
+    } else {
+      if ((st = set_smem(k_encode_kv<2>, kEncSmemBytes)) != SKV_OK) return st;
+      k_encode_kv<2><<<blocks, threads, kEncSmemBytes, s>>>(a);
+    }
+  }
+  if ((st = launch_check()) != SKV_OK) return st;
+  unsigned long long* part = reinterpret_cast<unsigned long long*>(ws + wl.part_off);
+  k_scan_reduce<<<(unsigned)wl.n_scan_blocks, 256, 0, s>>>(a.lane_words, g.n_lanes, part);
+  k_scan_parts<<<1, 1024, 0, s>>>(part, wl.n_scan_blocks);
+  k_scan_write<<<(unsigned)wl.n_scan_blocks, 256, 0, s>>>(a.lane_words, g.n_lanes, part, d_lane_offsets);
+  if ((st = launch_check()) != SKV_OK) return st;
+  if (h_total_bytes) {
+    uint64_t total = 0;
+    st = cuda_status(cudaMemcpyAsync(&total, d_lane_offsets + g.n_lanes, 8, cudaMemcpyDeviceToHost, s));
+    if (st == SKV_OK) st = cuda_status(cudaStreamSynchronize(s));
+    if (st != SKV_OK) return st;
+    *h_total_bytes = total;
+    if (total > cap_bytes) return SKV_ERR_CAPACITY;
+  }
+  {
+    int sms = sm_count();
+    uint64_t nb = (g.n_lanes + 7) / 8;
+    uint64_t cap_blocks = (uint64_t)(sms > 0 ? sms : 1) * 16;
+    k_compact<<<(unsigned)(nb < cap_blocks ? nb : cap_blocks), 256, 0, s>>>(
+        a.slots, a.lane_words, d_lane_offsets, g.n_lanes, g.slot_words, static_cast<uint8_t*>(d_bitstream),
+        cap_bytes, d_status);
+  }
+  return launch_check();
+}
+
+int skv_decode(const skv_params* p, const void* d_bitstream, uint64_t n_bytes, const uint64_t* d_lane_offsets,
+               const void* d_pred, const void* d_tables, const uint8_t* d_bins, void* d_target_out,
+               uint32_t* d_status, void* stream) {
+  Geo g;
+  int st = make_geo(p, &g);
+  if (st != SKV_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!d_status || ((uintptr_t)d_status & 3)) return SKV_ERR_INVALID_ARG;
+  st = cuda_status(cudaMemsetAsync(d_status, 0, 4, s));
+  if (st != SKV_OK || g.n_lanes == 0) return st;
+  if (!d_bitstream || !d_lane_offsets || !d_pred || !d_tables || !d_bins || !d_target_out)
+    return SKV_ERR_INVALID_ARG;
+  if (((uintptr_t)d_bitstream & 1) || ((uintptr_t)d_lane_offsets & 7) || !aligned16(d_pred) ||
+      !aligned16(d_tables) || !aligned16(d_bins) || !aligned16(d_target_out))
+    return SKV_ERR_INVALID_ARG;
+  CodecArgs a;
+  memset(&a, 0, sizeof(a));
+  a.prd = static_cast<const uint8_t*>(d_pred);
+  a.out = static_cast<uint8_t*>(d_target_out);
+  a.tables = static_cast<const uint8_t*>(d_tables);
+  a.bins = d_bins;
+  a.bs = static_cast<const uint8_t*>(d_bitstream);
+  a.offs = d_lane_offsets;
+  a.n_bytes = n_bytes;
+  a.status = d_status;
+  a.n_chunks = g.n_chunks;
+  a.cps = g.cps;
+  a.slice_pos = g.slice_pos;
+  a.n_lanes = g.n_lanes;
+  a.K = g.K;
+  a.D = g.D;
+  a.C = g.C;
+  if (g.dtype == SKV_COEF_I16) {
+    int sms = sm_count();
+    uint64_t nb = (g.n_chunks + 7) / 8;
+    uint64_t cap_blocks = (uint64_t)(sms > 0 ? sms : 1) * 8;
+    k_decode_coef<<<(unsigned)(nb < cap_blocks ? nb : cap_blocks), 256, 0, s>>>(a);
+    return launch_check();
+  }
+  int blocks, threads;
+  codec_grid(g.n_chunks, &blocks, &threads);
+  if (g.esz == 1) {
+    if ((st = set_smem(k_decode_kv<1>, kDecSmemBytes)) != SKV_OK) return st;
+    k_decode_kv<1><<<blocks, threads, kDecSmemBytes, s>>>(a);
+  } else {
+    if ((st = set_smem(k_decode_kv<2>, kDecSmemBytes)) != SKV_OK) return st;
+    k_decode_kv<2><<<blocks, threads, kDecSmemBytes, s>>>(a);
+  }
+  return launch_check();
+}
+
+int skv_read_status(const uint32_t* d_status, void* stream) {
+  if (!d_status) return SKV_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  int st = cuda_status(cudaMemcpyAsync(&v, d_status, 4, cudaMemcpyDeviceToHost, s));
+  if (st == SKV_OK) st = cuda_status(cudaStreamSynchronize(s));
+  if (st != SKV_OK) return st;
+  if (v & SKV_FLAG_CORRUPT) return SKV_ERR_CORRUPT;
+  if (v & SKV_FLAG_CAPACITY) return SKV_ERR_CAPACITY;
+  if (v & SKV_FLAG_TIMEOUT) return SKV_ERR_TIMEOUT;
+  if (v & SKV_FLAG_BAD_BIN) return SKV_ERR_INVALID_ARG;
+  return SKV_OK;
+}
+
+}  // extern "C"

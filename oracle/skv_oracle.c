@@ -458,6 +458,14 @@ static uint32_t dec_find(const or_dec *d, uint32_t prob_bits, const uint32_t *cu
   return i;
 }
 
+/* same search over a 16-bit cumulative table (the stream tables) */
+static uint32_t dec_find16(const or_dec *d, const uint16_t *cum) {
+  uint64_t slot = d->x & (PROB_SCALE - 1);
+  uint32_t i = 0;
+  while (i + 1 < NSYM && cum[i + 1] <= slot) i++;
+  return i;
+}
+
 /* Generic coder over an arbitrary table, for hand-worked examples and brute
  * force: encodes syms[0..n) (decode order) into one lane stream. */
 int or_rans_encode(uint32_t prob_bits, const uint32_t *freq, const uint32_t *cum,
@@ -576,7 +584,6 @@ int or_decode_chunk(const or_params *p, uint64_t chunk, const uint16_t *freq_all
   uint32_t esz = elem_bytes(p), width = 8u * esz, rb = raw_bytes(p);
   uint64_t start = 0;
   int status = OR_OK;
-  uint32_t cum32[NSYM + 1];
   uint64_t *pos_buf = (uint64_t *)malloc(p->lane_syms * sizeof(uint64_t));
   if (!pos_buf) return OR_ERR_ARG;
   for (uint32_t l = 0; l < LANES; l++) {
@@ -597,8 +604,7 @@ int or_decode_chunk(const or_params *p, uint64_t chunk, const uint16_t *freq_all
       }
       const uint16_t *fr = freq_all + (uint64_t)table * NSYM;
       const uint16_t *cm = cum_all + (uint64_t)table * (NSYM + 1);
-      for (uint32_t i = 0; i <= NSYM; i++) cum32[i] = cm[i];
-      uint32_t sym = dec_find(&d, PROB_BITS, cum32, NSYM);
+      uint32_t sym = dec_find16(&d, cm);
       dec_advance(&d, PROB_BITS, fr[sym], cm[sym]);
       uint64_t r;                         /* residual mod 2^width */
       if (sym == ESC) {

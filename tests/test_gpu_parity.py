@@ -1,0 +1,313 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Bit-exact comparisons (integer path): calibration bins / sums / histograms, every
+table's frequencies and cumulative frequencies, bitstream bytes, lane offsets and
+decoded caches.  Small shapes compare everything; the full-size workloads compare
+everything that the oracle finishes in seconds and otherwise sampled chunks (the
+oracle codes a chunk from that chunk's own data), plus decode(encode(x)) == x on
+the whole cache, which holds at any size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from lossless_kv_cache_fp8_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nat():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    from lossless_kv_cache_fp8_gb300 import native
+    return native
+
+
+def oparams(w):
+    if w.dtype == synth.COEF:
+        return oracle.coef_params(w.n_tokens, w.n_coef, w.lane_syms)
+    return oracle.kv_params(w.dtype, w.n_layers, w.n_kv, w.n_heads, w.head_dim, w.n_tokens, w.lane_syms,
+                            w.n_calib)
+
+
+def host_bits(x: torch.Tensor) -> np.ndarray:
+    a = x.detach().cpu().numpy().reshape(-1)
+    if a.dtype == np.int16:
+        return a.view(np.uint16)
+    return a
+
+
+def table_arrays(nat, codec):
+    blob = codec.tables.cpu().numpy()
+    nt = codec.sz["tables"]
+    blob = blob[: nt * nat.SKV_TABLE_STRIDE].reshape(nt, nat.SKV_TABLE_STRIDE)
+    fr = blob[:, nat.SKV_TABLE_FREQ_OFF:nat.SKV_TABLE_FREQ_OFF + 512].copy().view(np.uint16)
+    cum = blob[:, nat.SKV_TABLE_CUM_OFF:nat.SKV_TABLE_CUM_OFF + 514].copy().view(np.uint16)
+    return blob, fr, cum
+
+
+def run_gpu(nat, w, t, p, c, cap=None):
+    codec = nat.Codec(nat.params_for(w), bitstream_capacity=cap)
+    codec.calibrate(None if w.dtype == synth.COEF else t, c)
+    codec.build_tables()
+    total = codec.encode(t, p)
+    assert codec.check() == nat.SKV_OK
+    out = torch.empty_like(t)
+    codec.decode(p, out)
+    assert codec.check() == nat.SKV_OK
+    return codec, total, out
+
+
+SMALL = [
+    synth.WORKLOADS["qwen3-0.6b-1k-fp8"].scaled(n_layers=2, n_tokens=512),
+    synth.WORKLOADS["qwen3-0.6b-8k-bf16"].scaled(n_layers=1, n_tokens=384),
+    synth.WORKLOADS["qwen3-8b-32k-fp8"].scaled(n_layers=1, n_heads=2, n_tokens=1024, lane_syms=256),
+    synth.WORKLOADS["hybrid-coef-32k-x2048"].scaled(n_tokens=64, n_coef=256, lane_syms=64),
+    # ragged: tokens not a multiple of the chunk, fewer tokens than calibration, odd head dims
+    synth.WORKLOADS["qwen3-0.6b-1k-fp8"].scaled(n_layers=1, n_heads=3, n_tokens=77, head_dim=32, lane_syms=48),
+    synth.WORKLOADS["qwen3-0.6b-1k-fp8"].scaled(n_layers=1, n_heads=1, n_tokens=1000, head_dim=16, lane_syms=16),
+    synth.WORKLOADS["qwen3-0.6b-8k-bf16"].scaled(n_layers=1, n_heads=1, n_tokens=1, head_dim=16, lane_syms=8),
+    synth.WORKLOADS["qwen3-0.6b-8k-bf16"].scaled(n_layers=2, n_heads=2, n_tokens=300, head_dim=256, lane_syms=40),
+    synth.WORKLOADS["hybrid-coef-32k-x2048"].scaled(n_tokens=7, n_coef=37, lane_syms=24),
+    synth.WORKLOADS["hybrid-coef-32k-x2048"].scaled(n_tokens=33, n_coef=3, lane_syms=8),
+]
+
+
+def full_compare(nat, w):
+    t, p, c = synth.gen_workload(w, "cpu")
+    td, pd, cd = t.cuda(), p.cuda(), c.cuda()
+    codec, total, out = run_gpu(nat, w, td, pd, cd)
+    assert torch.equal(out, td)
+    po = oparams(w)
+    tn, pn, cn = host_bits(t), host_bits(p), c.numpy().reshape(-1) if w.dtype == synth.COEF else host_bits(c)
+    if w.dtype == synth.COEF:
+        tn = t.numpy().reshape(-1)
+        pn = p.numpy().reshape(-1)
+        bins, _, _ = oracle.calibrate(po, None, cn)
+    else:
+        bins, sums, _ = oracle.calibrate(po, tn, cn)
+    nch = bins.size
+    assert np.array_equal(codec.bins[:nch].cpu().numpy(), bins)
+    fr, cum = oracle.build_tables(po)
+    _, gfr, gcum = table_arrays(nat, codec)
+    assert np.array_equal(gfr, fr) and np.array_equal(gcum, cum)
+    st, bs, offs = oracle.encode(po, fr, cum, bins, tn, pn)
+    assert st == oracle.OK
+    assert total == bs.size
+    assert np.array_equal(codec.lane_offsets.cpu().numpy().astype(np.uint64), offs)
+    assert np.array_equal(codec.bitstream[:total].cpu().numpy(), bs)
+    return codec
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: f"{w.name}-L{w.n_layers}H{w.n_heads}T{w.n_tokens}D{w.head_dim}K{w.lane_syms}")
+def test_small_bit_exact(nat, w):
+    full_compare(nat, w)
+
+
+def test_calibration_sums_and_histograms(nat):
+    w = synth.WORKLOADS["qwen3-0.6b-1k-fp8"].scaled(n_layers=1, n_tokens=600)
+    t, p, _ = synth.gen_workload(w, "cpu")
+    po = oparams(w)
+    bins, sums, hist = oracle.calibrate(po, host_bits(t), host_bits(p), want_sum=True, want_hist=True)
+    codec = nat.Codec(nat.params_for(w))
+    s_d = torch.zeros(bins.size, dtype=torch.int32, device="cuda")
+    h_d = torch.zeros(bins.size * 256, dtype=torch.int32, device="cuda")
+    codec.calibrate(t.cuda(), p.cuda(), sum_abs=s_d, hist=h_d)
+    torch.cuda.synchronize()
+    assert np.array_equal(codec.bins[: bins.size].cpu().numpy(), bins)
+    assert np.array_equal(s_d.cpu().numpy().view(np.uint32), sums)
+    assert np.array_equal(h_d.cpu().numpy().view(np.uint32).reshape(-1, 256), hist)
+
+
+@pytest.mark.parametrize("kind", ["kv", "coef"])
+def test_table_blob_structures(nat, kind):
+    """encoder reciprocals, slot->symbol tables and decoder entries are consistent
+    with the frequencies (checked on the host from their definitions)"""
+    p = nat.kv_params(1, 1, 2, 1, 128, 16, 16) if kind == "kv" else nat.coef_params(4, 16, 8)
+    codec = nat.Codec(p)
+    codec.build_tables()
+    torch.cuda.synchronize()
+    blob, fr, cum = table_arrays(nat, codec)
+    for t in range(blob.shape[0]):
+        f = fr[t].astype(np.int64)
+        c = cum[t].astype(np.int64)
+        enc = blob[t, nat.SKV_TABLE_ENC_OFF:nat.SKV_TABLE_ENC_OFF + 4096].copy().view(np.uint32).reshape(256, 4)
+        m = enc[:, 0].astype(object) + (enc[:, 1].astype(object) << 32)
+        for i in range(256):
+            fi = int(f[i])
+            assert m[i] == -(-(1 << 44) // fi)
+            # floor(x/fr) = floor(x m / 2^44) for all x < fr 2^20: error term (fr 2^20 - 1)(m fr - 2^44) < 2^44
+            assert (fi * (1 << 20) - 1) * (m[i] * fi - (1 << 44)) < (1 << 44)
+        assert np.array_equal(enc[:, 2], (f << 20).astype(np.uint32))
+        assert np.array_equal(enc[:, 3], ((4096 - f) | (c[:256] << 16)).astype(np.uint32))
+        dec = blob[t, nat.SKV_TABLE_DEC_OFF:nat.SKV_TABLE_DEC_OFF + 1024].copy().view(np.uint32)
+        assert np.array_equal(dec, (f | (c[:256] << 16)).astype(np.uint32))
+        lut = blob[t, nat.SKV_TABLE_LUT_OFF:nat.SKV_TABLE_LUT_OFF + 4096]
+        assert np.array_equal(lut, np.repeat(np.arange(256), f).astype(np.uint8))
+
+
+FULL_EXACT = ["qwen3-0.6b-1k-fp8", "hybrid-coef-32k-x2048"]
+
+
+@pytest.mark.parametrize("name", FULL_EXACT)
+def test_full_size_bit_exact(nat, name):
+    """whole workloads the oracle codes in seconds: every byte compared"""
+    full_compare(nat, synth.WORKLOADS[name])
+
+
+def sampled_compare(nat, w, n_samples=6, seed=0):
+    """generate on the GPU, code the whole cache there, compare sampled chunks
+    (first, last and random ones) with the oracle coding those chunks"""
+    t, p, c = synth.gen_workload(w, "cuda")
+    codec = nat.Codec(nat.params_for(w), bitstream_capacity=w.raw_bytes)
+    codec.calibrate(t, c)
+    codec.build_tables()
+    total = codec.encode(t, p)
+    assert codec.check() == nat.SKV_OK
+    out = torch.empty_like(t)
+    codec.decode(p, out)
+    assert codec.check() == nat.SKV_OK
+    assert torch.equal(out, t)
+    del out
+    po = oparams(w)
+    g = oracle.geometry(po)
+    fr, cum = oracle.build_tables(po)
+    _, gfr, gcum = table_arrays(nat, codec)
+    assert np.array_equal(gfr, fr) and np.array_equal(gcum, cum)
+    rng = np.random.default_rng(seed)
+    chunks = sorted({0, g["n_chunks"] - 1, *rng.integers(0, g["n_chunks"], n_samples).tolist()})
+    offs = codec.lane_offsets.cpu().numpy().astype(np.int64)
+    assert offs[0] == 0 and offs[-1] == total and np.all(np.diff(offs) >= 4)
+    tflat, pflat = t.view(-1), p.view(-1)
+    gbins = codec.bins[: g["n_channels"]].cpu().numpy()
+    sp, cs = g["slice_positions"], 32 * w.lane_syms
+    D = w.head_dim
+    for ch in chunks:
+        sl, k = divmod(ch, g["chunks_per_slice"])
+        first = sl * sp + k * cs
+        n_pos = min(cs, sp - k * cs)
+        # calibration of this slice by the oracle, from the slice's own first tokens
+        ncal = min(w.n_calib, w.n_tokens)
+        s0 = sl * sp
+        po1 = oracle.kv_params(w.dtype, 1, 1, 1, D, ncal, w.lane_syms, w.n_calib)
+        b1, _, _ = oracle.calibrate(po1, host_bits(tflat[s0:s0 + ncal * D]), host_bits(pflat[s0:s0 + ncal * D]))
+        assert np.array_equal(gbins[sl * D:(sl + 1) * D], b1), f"bins of slice {sl}"
+        tc = host_bits(tflat[first:first + n_pos])
+        pc = host_bits(pflat[first:first + n_pos])
+        words, lw = oracle.encode_chunk(po, ch, fr, cum, gbins, tc, pc)
+        a, b = offs[32 * ch], offs[32 * ch + 32]
+        got = codec.bitstream[a:b].cpu().numpy().view(np.uint16)
+        assert np.array_equal(got, words), f"chunk {ch}"
+        assert np.array_equal(np.diff(offs[32 * ch:32 * ch + 33]) // 2, lw.astype(np.int64))
+    return codec, total
+
+
+@pytest.mark.parametrize("name", ["qwen3-0.6b-8k-bf16", "qwen3-8b-32k-fp8", "qwen3-32b-128k-fp8"])
+def test_full_size_sampled(nat, name):
+    w = synth.WORKLOADS[name]
+    free, _ = torch.cuda.mem_get_info()
+    need = 2 * w.raw_bytes + w.raw_bytes + nat.sizes(nat.params_for(w))["workspace"] + w.raw_bytes
+    if need > free:
+        pytest.skip(f"needs {need / 1e9:.0f} GB of device memory, {free / 1e9:.0f} GB free")
+    codec, total = sampled_compare(nat, w)
+    ratio = w.raw_bytes / (total + 4 * codec.sz["lanes"] + codec.sz["channels"] + 64)
+    print(f"{name}: {w.raw_bytes / 1e9:.2f} GB -> {total / 1e9:.3f} GB, ratio {ratio:.3f}")
+    del codec
+    torch.cuda.empty_cache()
+
+
+def test_oracle_decodes_gpu_stream(nat):
+    w = SMALL[1]
+    codec = full_compare(nat, w)
+    t, p, c = synth.gen_workload(w, "cpu")
+    po = oparams(w)
+    bins = codec.bins[: oracle.geometry(po)["n_channels"]].cpu().numpy()
+    fr, cum = oracle.build_tables(po)
+    bs = codec.bitstream[: codec.n_bytes].cpu().numpy()
+    st, out = oracle.decode(po, fr, cum, bins, bs, codec.lane_offsets.cpu().numpy().astype(np.uint64),
+                            host_bits(p), np.uint16)
+    assert st == oracle.OK and np.array_equal(out, host_bits(t))
+
+
+def test_deterministic(nat):
+    w = SMALL[0]
+    t, p, c = synth.gen_workload(w, "cuda")
+    c1, n1, _ = run_gpu(nat, w, t, p, c)
+    c2, n2, _ = run_gpu(nat, w, t, p, c)
+    assert n1 == n2 and torch.equal(c1.bitstream[:n1], c2.bitstream[:n2])
+
+
+def test_corrupt_streams_reported(nat):
+    w = SMALL[0]
+    t, p, c = synth.gen_workload(w, "cuda")
+    codec, total, _ = run_gpu(nat, w, t, p, c)
+    out = torch.empty_like(t)
+    # damaged state words of one lane
+    bs = codec.bitstream.clone()
+    a = int(codec.lane_offsets[7])
+    bs[a + 1] ^= 0x40
+    codec.decode(p, out, bitstream=bs)
+    assert codec.check() == nat.SKV_ERR_CORRUPT
+    # stream shorter than the offsets say
+    codec.decode(p, out, n_bytes=total - 2)
+    assert codec.check() == nat.SKV_ERR_CORRUPT
+    # offsets out of order
+    lo = codec.lane_offsets.clone()
+    lo[3], lo[4] = codec.lane_offsets[4].item(), codec.lane_offsets[3].item()
+    codec.decode(p, out, lane_offsets=lo)
+    assert codec.check() == nat.SKV_ERR_CORRUPT
+    # the intact stream still decodes
+    codec.decode(p, out)
+    assert codec.check() == nat.SKV_OK and torch.equal(out, t)
+
+
+def test_capacity(nat):
+    w = SMALL[0]
+    t, p, c = synth.gen_workload(w, "cuda")
+    codec = nat.Codec(nat.params_for(w), bitstream_capacity=64)
+    codec.calibrate(t, c)
+    codec.build_tables()
+    st, tot = nat.skv_encode(codec.p, t, p, codec.tables, codec.bins, codec.bitstream, codec.cap,
+                             codec.lane_offsets, codec.workspace, codec.workspace.numel(), codec.status)
+    assert st == nat.SKV_ERR_CAPACITY and tot > 64
+    st, _ = nat.skv_encode(codec.p, t, p, codec.tables, codec.bins, codec.bitstream, codec.cap,
+                           codec.lane_offsets, codec.workspace, codec.workspace.numel(), codec.status,
+                           want_total=False)
+    assert st == nat.SKV_OK
+    assert codec.check() == nat.SKV_ERR_CAPACITY
+
+
+def test_argument_errors(nat):
+    w = SMALL[0]
+    t, p, c = synth.gen_workload(w, "cuda")
+    codec = nat.Codec(nat.params_for(w))
+    raw = torch.empty(t.numel() + 16, dtype=torch.uint8, device="cuda")
+    st = nat.skv_calibrate(codec.p, raw.data_ptr() + 1, p, codec.bins)
+    assert st == nat.SKV_ERR_INVALID_ARG
+    codec.calibrate(t, c)
+    codec.build_tables()
+    st, _ = nat.skv_encode(codec.p, t, p, codec.tables, codec.bins, codec.bitstream, codec.cap,
+                           codec.lane_offsets, codec.workspace, 16, codec.status)
+    assert st == nat.SKV_ERR_INVALID_ARG                  # workspace too small
+    bad = codec.bins.clone()
+    bad[5] = 200                                          # out-of-range bin
+    st, _ = nat.skv_encode(codec.p, t, p, codec.tables, bad, codec.bitstream, codec.cap,
+                           codec.lane_offsets, codec.workspace, codec.workspace.numel(), codec.status)
+    assert st == nat.SKV_OK
+    assert codec.check() == nat.SKV_ERR_INVALID_ARG
+
+
+def test_empty(nat):
+    p = nat.kv_params(1, 2, 2, 2, 128, 0, 1024)
+    codec = nat.Codec(p)
+    t = torch.empty(16, dtype=torch.uint8, device="cuda")
+    codec.calibrate(t, t)
+    codec.build_tables()
+    assert codec.encode(t, t) == 0
+    assert int(codec.lane_offsets[0]) == 0
+    codec.decode(t, t)
+    assert codec.check() == nat.SKV_OK
