@@ -211,12 +211,15 @@ def main_ours(args):
     dev = torch.device("cuda", local)
     libbuild.build()
     w = synth.WORKLOADS[args.workload]
+    if args.layers:
+        w = w.scaled(n_layers=args.layers)
     p = native.params_for(w)
     sz = native.sizes(p)
     stream = torch.cuda.current_stream(dev)
 
     # inputs resident in HBM before the timed region
     tgt, prd, cal = synth.gen_workload(w, dev)
+    torch.cuda.empty_cache()
     codec = native.Codec(p, device=dev, bitstream_capacity=int(w.raw_bytes * args.cap_frac))
     out = torch.empty_like(tgt)
     torch.cuda.synchronize()
@@ -356,6 +359,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling cases)")
     ap.add_argument("--cap-frac", type=float, default=0.6, help="bitstream buffer / raw bytes")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--e2e-steps", type=int, default=3)
