@@ -177,6 +177,32 @@ int skv_decode(const skv_params* p, const void* d_bitstream, uint64_t n_bytes,
                const uint64_t* d_lane_offsets, const void* d_pred, const void* d_tables,
                const uint8_t* d_bins, void* d_target_out, uint32_t* d_status, void* stream);
 
+/* Encode without a caller-provided workspace.  The pages have no counterpart
+ * to this call; it exists for callers that cannot allocate device memory, such
+ * as code handed only its input and output buffers by a host framework that
+ * owns every allocation, or code running where the device's memory has already
+ * been claimed by another pool and a cudaMalloc would fail.
+ *
+ * Same arguments and results as skv_encode minus the workspace.  The scratch
+ * is a file-scope device array of SKV_NOALLOC_SCRATCH_BYTES (64 MiB) inside
+ * libskv.so, which every GPU that loads the library holds until the process
+ * exits.  Streams whose skv_encode_workspace_bytes exceeds that size are
+ * rejected with SKV_ERR_UNSUPPORTED before anything is launched (for FP8 with
+ * lane_syms 1024 the limit is about 16 million positions).
+ *
+ * The first call on a device looks up the array's device address on the
+ * current device (once per device, then cached); make that first call before
+ * any stream capture.  The call itself allocates nothing and frees nothing.
+ * Every call on a device shares the one array and it keeps the last call's
+ * contents; nothing in it needs clearing, because the encoder writes every
+ * scratch word before reading it.  Calls whose work overlaps on the GPU
+ * (different streams, or other host threads) race on the array: serialise them. */
+#define SKV_NOALLOC_SCRATCH_BYTES (64ull << 20)
+int skv_encode_noalloc(const skv_params* p, const void* d_target, const void* d_pred,
+                       const void* d_tables, const uint8_t* d_bins, void* d_bitstream,
+                       uint64_t cap_bytes, uint64_t* d_lane_offsets, uint32_t* d_status,
+                       uint64_t* h_total_bytes, void* stream);
+
 /* Synchronises the stream, reads the status word and returns SKV_OK or the
  * code of the most serious flag (CORRUPT > CAPACITY > TIMEOUT > INVALID_ARG
  * for an out-of-range bin). */

@@ -35,6 +35,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "skv.h"
 
 namespace {
@@ -1084,6 +1086,41 @@ int skv_decode(const skv_params* p, const void* d_bitstream, uint64_t n_bytes, c
     k_decode_kv<2><<<blocks, threads, kDecSmemBytes, s>>>(a);
   }
   return launch_check();
+}
+
+// Scratch of skv_encode_noalloc: a file-scope device array, so the call never
+// allocates.  Host code cannot use the symbol itself as a device address; the
+// address is looked up once per device with cudaGetSymbolAddress.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[SKV_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 128;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices];
+}  // namespace
+
+int skv_encode_noalloc(const skv_params* p, const void* d_target, const void* d_pred, const void* d_tables,
+                       const uint8_t* d_bins, void* d_bitstream, uint64_t cap_bytes, uint64_t* d_lane_offsets,
+                       uint32_t* d_status, uint64_t* h_total_bytes, void* stream) {
+  Geo g;
+  int st = make_geo(p, &g);
+  if (st != SKV_OK) return st;
+  if (ws_layout(g).total > SKV_NOALLOC_SCRATCH_BYTES) return SKV_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SKV_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return SKV_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return SKV_ERR_CUDA;
+      g_noalloc_ptr[dev] = ptr;
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  return skv_encode(p, d_target, d_pred, d_tables, d_bins, d_bitstream, cap_bytes, d_lane_offsets, scratch,
+                    SKV_NOALLOC_SCRATCH_BYTES, d_status, h_total_bytes, stream);
 }
 
 int skv_read_status(const uint32_t* d_status, void* stream) {

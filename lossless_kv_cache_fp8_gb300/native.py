@@ -71,6 +71,8 @@ _SIGS = {
                              C.c_void_p, C.c_void_p, C.c_uint64, C.c_void_p, C.c_void_p, C.c_void_p]),
     "skv_decode": (C.c_int, [_P, C.c_void_p, C.c_uint64, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                              C.c_void_p, C.c_void_p, C.c_void_p]),
+    "skv_encode_noalloc": (C.c_int, [_P, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                     C.c_uint64, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
     "skv_read_status": (C.c_int, [C.c_void_p, C.c_void_p]),
 }
 
@@ -156,6 +158,17 @@ def skv_encode(p, target, pred, tables, bins, bitstream, cap_bytes, lane_offsets
     st = lib().skv_encode(C.byref(p), _ptr(target), _ptr(pred), _ptr(tables), _ptr(bins), _ptr(bitstream),
                           cap_bytes, _ptr(lane_offsets), _ptr(workspace), workspace_bytes, _ptr(status),
                           C.byref(tot) if want_total else None, _stream(stream))
+    return st, (tot.value if want_total else None)
+
+
+def skv_encode_noalloc(p, target, pred, tables, bins, bitstream, cap_bytes, lane_offsets, status,
+                       want_total=True, stream=None):
+    """Encode with the library's own static scratch (no workspace argument).
+    Returns (status_code, total_bytes or None)."""
+    tot = C.c_uint64(0)
+    st = lib().skv_encode_noalloc(C.byref(p), _ptr(target), _ptr(pred), _ptr(tables), _ptr(bins), _ptr(bitstream),
+                                  cap_bytes, _ptr(lane_offsets), _ptr(status),
+                                  C.byref(tot) if want_total else None, _stream(stream))
     return st, (tot.value if want_total else None)
 
 
