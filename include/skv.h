@@ -13,7 +13,9 @@
  * Conventions for every call:
  *   - Pointers prefixed d_ are device memory owned by the caller; h_ pointers
  *     are host memory.  The library allocates nothing and frees nothing.
- *   - Device buffers must be 16-byte aligned (cudaMalloc gives 256).
+ *   - Device buffers must be 16-byte aligned (cudaMalloc gives 256), and a
+ *     bitstream buffer must be readable up to the next multiple of 16 bytes
+ *     past its end (the decoder reads whole aligned 16-byte blocks).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls enqueue their kernels on it and return without waiting,
  *     except where a call says it synchronises.
@@ -78,21 +80,23 @@ extern "C" {
 
 /* Table blob: table t occupies SKV_TABLE_STRIDE bytes at t*SKV_TABLE_STRIDE.
  * Within a table:
- *   SKV_TABLE_ENC_OFF  256 x {u32 m_lo, u32 m_hi, u32 fr<<20, u32 (4096-fr) | cum<<16}
- *                      encoder entries; floor(x/fr) = (umulhi(x,m_lo) + x*m_hi) >> 12
- *                      with m = ceil(2^44/fr), exact for every state the coder meets
+ *   SKV_TABLE_ENC_OFF  256 x {u32 m_lo, u32 w}: encoder entries with
+ *                      w = fr << 20 | cum << 8 | h << 7 | s, where
+ *                      m = h*2^32 + m_lo = ceil(2^(32+s) / fr) and
+ *                      floor(x / fr) = (umulhi(x, m_lo) + h*x) >> s
+ *                      exactly for every state x < fr*2^20 the encoder meets
  *   SKV_TABLE_LUT_OFF  4096 x u8: symbol owning each 12-bit slot
  *   SKV_TABLE_DEC_OFF  256 x u32: fr | cum << 16
  *   SKV_TABLE_FREQ_OFF 256 x u16: frequencies (sum 4096, each >= 1)
  *   SKV_TABLE_CUM_OFF  257 x u16: cumulative frequencies (cum[256] = 4096)
  * KV streams have 32 tables (scale bin b = table b); COEF streams have 1024
  * (table 16*b + f: scale bin b, mean fraction f/16). */
-#define SKV_TABLE_STRIDE 12288u
+#define SKV_TABLE_STRIDE 8704u
 #define SKV_TABLE_ENC_OFF 0u
-#define SKV_TABLE_LUT_OFF 4096u
-#define SKV_TABLE_DEC_OFF 8192u
-#define SKV_TABLE_FREQ_OFF 9216u
-#define SKV_TABLE_CUM_OFF 9728u
+#define SKV_TABLE_LUT_OFF 2048u
+#define SKV_TABLE_DEC_OFF 6144u
+#define SKV_TABLE_FREQ_OFF 7168u
+#define SKV_TABLE_CUM_OFF 7680u
 
 /* Status-word bits set by kernels (skv_read_status maps them to codes). */
 #define SKV_FLAG_CORRUPT 1u

@@ -46,13 +46,21 @@ constexpr uint32_t kChain = 2056;        // tau^0 .. tau^2055 covers |16 s + 8 +
 constexpr uint32_t kStateLow = 1u << 16; // rANS state lower bound L
 constexpr uint32_t kKvTables = 32;
 constexpr uint32_t kCoefTables = 1024;
-// shared-memory strides per table, padded so that the same symbol of two
-// tables falls in different banks
-constexpr uint32_t kEncSmemStride = 4096 + 16;
-constexpr uint32_t kDecSmemStride = 4096 + 1024 + 4;
-constexpr uint32_t kEncSmemBytes = kKvTables * kEncSmemStride;
-constexpr uint32_t kDecSmemBytes = kKvTables * kDecSmemStride;
-constexpr int kCodecThreads = 1024;
+// Shared-memory layout of the codec kernels.  Table strides are padded so
+// that the same symbol of neighbouring tables falls in different banks:
+// encoder entries are 8 bytes (stride/8 = 5 mod 16), decoder tables are the
+// slot->symbol LUT followed by the 32-bit decoder entries (stride/4 = 5 mod 32).
+constexpr uint32_t kEncTabStride = 2048 + 40;
+constexpr uint32_t kEncTabBytes = kKvTables * kEncTabStride;       // 66816
+constexpr uint32_t kEmitBytes = 144;                               // per-lane word buffer
+constexpr uint32_t kEmitFlush = 80;                                // flush threshold (bytes)
+constexpr uint32_t kDecTabStride = 4096 + 1024 + 20;
+constexpr uint32_t kDecTabBytes = kKvTables * kDecTabStride;       // 164480
+constexpr uint32_t kRingBytes = 64;                                // per-lane stream ring
+#ifndef SKV_CODEC_THREADS
+#define SKV_CODEC_THREADS 1024
+#endif
+constexpr int kCodecThreads = SKV_CODEC_THREADS;   // threads per codec CTA (one CTA per SM)
 constexpr int kScanPerBlock = 4096;       // lanes per scan block (256 threads x 16)
 
 // ---------------------------------------------------------------------------
@@ -110,14 +118,31 @@ int make_geo(const skv_params* p, Geo* g) {
 
 uint64_t align256(uint64_t v) { return (v + 255) & ~255ull; }
 
+// Upper bound on resident codec warps (152 SMs x 32 warps fit; larger devices
+// are clamped to it).  KV encode scratch is one slot per lane of each warp.
+constexpr uint64_t kMaxWarps = 5120;
+
 struct WsLayout {
-  uint64_t slots_off, lw_off, part_off, total;
-  uint64_t n_scan_blocks;
+  uint64_t slots_off, lw_off, part_off, state_off, ticket_off, total;
+  uint64_t n_scan_blocks, n_slots;
 };
 
+// KV: per-warp lane slots (reused chunk after chunk) + chunk look-back states
+// + the chunk ticket.  COEF: per-lane slots + lane lengths + scan partials.
 WsLayout ws_layout(const Geo& g) {
   WsLayout w;
+  memset(&w, 0, sizeof(w));
+  if (g.dtype != SKV_COEF_I16) {
+    const uint64_t warps = g.n_chunks < kMaxWarps ? g.n_chunks : kMaxWarps;
+    w.n_slots = warps * kLanes;
+    w.slots_off = 0;
+    w.state_off = align256(w.n_slots * g.slot_words * 2);
+    w.ticket_off = w.state_off + align256(g.n_chunks * 8);
+    w.total = w.ticket_off + 256;
+    return w;
+  }
   w.n_scan_blocks = (g.n_lanes + kScanPerBlock - 1) / kScanPerBlock;
+  w.n_slots = g.n_lanes;
   w.slots_off = 0;
   w.lw_off = align256(g.n_lanes * g.slot_words * 2);
   w.part_off = w.lw_off + align256(g.n_lanes * 4);
@@ -153,18 +178,9 @@ __device__ __forceinline__ uint32_t unord16x2(uint32_t u) {
   return u ^ (((~u >> 15) & 0x00010001u) * 0x7FFFu | 0x80008000u);
 }
 
-__device__ __forceinline__ uint4 ldg_stream(const void* ptr) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(ptr));
-  return v;
-}
-__device__ __forceinline__ void stg_stream(void* ptr, uint4 v) {
-  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(ptr), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
-}
+// streaming (evict-first) 128-bit loads and stores of the caches
+__device__ __forceinline__ uint4 ldg_stream(const void* ptr) { return __ldcs(reinterpret_cast<const uint4*>(ptr)); }
+__device__ __forceinline__ void stg_stream(void* ptr, uint4 v) { __stcs(reinterpret_cast<uint4*>(ptr), v); }
 
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int k) {
   return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
@@ -180,17 +196,61 @@ __device__ __forceinline__ uint32_t bin_from_q(uint64_t q, uint32_t sub) {
   return sub * (pw - 13) + (uint32_t)((q >> (pw - sb)) & (sub - 1));
 }
 
-// encoder step with table entry {m_lo, m_hi, fr << 20, (4096 - fr) | cum << 16}
-__device__ __forceinline__ void enc_step(uint32_t& x, uint16_t*& wp, const uint4 e) {
-  if (x >= e.z) {
+// ---- shared-memory access by byte offset into the dynamic shared array -----
+// Plain C++ accesses (not volatile asm) so that the compiler may predicate and
+// schedule them like any other instruction.
+extern __shared__ __align__(16) uint8_t g_smem[];
+__device__ __forceinline__ void sts_u16(uint32_t a, uint32_t v) {
+  *reinterpret_cast<uint16_t*>(g_smem + a) = (uint16_t)v;
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) { return *reinterpret_cast<const uint16_t*>(g_smem + a); }
+__device__ __forceinline__ uint32_t lds_u8(uint32_t a) { return g_smem[a]; }
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) { return *reinterpret_cast<const uint32_t*>(g_smem + a); }
+__device__ __forceinline__ uint2 lds_u64(uint32_t a) { return *reinterpret_cast<const uint2*>(g_smem + a); }
+__device__ __forceinline__ uint4 lds_u128(uint32_t a) { return *reinterpret_cast<const uint4*>(g_smem + a); }
+__device__ __forceinline__ void sts_u128(uint32_t a, uint4 v) { *reinterpret_cast<uint4*>(g_smem + a) = v; }
+__device__ __forceinline__ void stg_u128(void* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
+
+// Encoder entry {m_lo, w}, w = fr << 20 | cum << 8 | h << 7 | s:
+// floor(x / fr) = (umulhi(x, m_lo) + (h ? x : 0)) >> s.
+// prmt with selector 0x8888 replicates the sign bit of byte 0 (= h) into a mask.
+__device__ __forceinline__ uint32_t enc_quot(uint32_t x, uint32_t m_lo, uint32_t w) {
+  uint32_t hmask;
+  asm("prmt.b32 %0, %1, 0, 0x8888;" : "=r"(hmask) : "r"(w));
+  const uint32_t t = __umulhi(x, m_lo) + (x & hmask);
+  return __funnelshift_r(t, 0u, w);   // shift amount = w & 31 = s
+}
+
+// one coding step; renormalisation words go to a downward-growing buffer
+// addressed by rp (shared-window byte address)
+__device__ __forceinline__ void enc_step_smem(uint32_t& x, uint32_t& rp, uint2 e) {
+  if (x >= (e.y & 0xFFF00000u)) {
+    rp -= 2;
+    sts_u16(rp, x);
+    x >>= 16;
+  }
+  const uint32_t q = enc_quot(x, e.x, e.y);
+  x = x + q * (4096u - (e.y >> 20)) + ((e.y >> 8) & 0xFFFu);
+}
+// raw byte v as a uniform step (fr 16, cum 16 v)
+__device__ __forceinline__ void enc_raw_smem(uint32_t& x, uint32_t& rp, uint32_t v) {
+  if (x >= (1u << 24)) {
+    rp -= 2;
+    sts_u16(rp, x);
+    x >>= 16;
+  }
+  x = ((x >> 4) << 12) | (x & 15u) | (v << 4);
+}
+// the same with words written downward straight into global scratch (COEF path)
+__device__ __forceinline__ void enc_step_gmem(uint32_t& x, uint16_t*& wp, uint2 e) {
+  if (x >= (e.y & 0xFFF00000u)) {
     *--wp = (uint16_t)x;
     x >>= 16;
   }
-  const uint32_t q = (__umulhi(x, e.x) + x * e.y) >> 12;   // floor(x / fr)
-  x = x + q * (e.w & 0xFFFFu) + (e.w >> 16);
+  const uint32_t q = enc_quot(x, e.x, e.y);
+  x = x + q * (4096u - (e.y >> 20)) + ((e.y >> 8) & 0xFFFu);
 }
-// raw byte v as a uniform step: fr 16, cum 16 v
-__device__ __forceinline__ void enc_raw(uint32_t& x, uint16_t*& wp, uint32_t v) {
+__device__ __forceinline__ void enc_raw_gmem(uint32_t& x, uint16_t*& wp, uint32_t v) {
   if (x >= (1u << 24)) {
     *--wp = (uint16_t)x;
     x >>= 16;
@@ -198,6 +258,7 @@ __device__ __forceinline__ void enc_raw(uint32_t& x, uint16_t*& wp, uint32_t v) 
   x = ((x >> 4) << 12) | (x & 15u) | (v << 4);
 }
 
+// Decoder lane reading its words straight from global memory (COEF path).
 struct DecLane {
   const uint16_t* w;
   uint32_t n, p, nxt, x;
@@ -231,6 +292,80 @@ __device__ __forceinline__ void dec_open(DecLane& L, const uint8_t* bs, uint64_t
 }
 __device__ __forceinline__ void dec_close(const DecLane& L, uint32_t* status) {
   if (L.x != kStateLow || L.p != L.n) atomicOr(status, SKV_FLAG_CORRUPT);
+}
+
+// Decoder lane reading its words through a 64-byte shared-memory ring of
+// aligned 16-byte stream blocks (block k lives in ring slot k mod 4).  The
+// block after the ring is staged in registers one refill ahead.  Offsets are
+// relative to base = the lane's first byte rounded down to 64, so the ring
+// index of byte offset p is p & 63.
+struct RingLane {
+  const uint8_t* base; // bitstream + (lane start & ~63)
+  uint32_t ring;       // shared-window address of the ring (64-byte aligned)
+  uint32_t p;          // next word to consume
+  uint32_t end;        // one past the lane's last byte
+  uint32_t rb;         // next block to move into the ring
+  uint32_t last;       // last block holding lane bytes (rb > last: nothing left)
+  uint4 stage;         // block rb, loaded ahead
+  uint32_t nxt, x;
+};
+__device__ __forceinline__ uint4 load_block(const RingLane& L, uint32_t k) {
+  return k <= L.last ? ldg_stream(L.base + ((uint64_t)k << 4)) : make_uint4(0, 0, 0, 0);
+}
+// make blocks [p/16, p/16 + 4) resident
+__device__ __forceinline__ void ring_refill(RingLane& L) {
+  const uint32_t need = (L.p >> 4) + 4;
+  while (L.rb < need) {
+    sts_u128(L.ring + (L.rb & 3u) * 16u, L.stage);
+    ++L.rb;
+    L.stage = load_block(L, L.rb);
+  }
+}
+__device__ __forceinline__ uint32_t ring_word(const RingLane& L, uint32_t p) {
+  return lds_u16(L.ring + (p & 63u));
+}
+__device__ __forceinline__ void ring_renorm(RingLane& L) {
+  if (L.x < kStateLow) {
+    L.x = (L.x << 16) | L.nxt;
+    L.p += 2;
+    L.nxt = ring_word(L, L.p);
+  }
+}
+__device__ __forceinline__ uint32_t ring_raw(RingLane& L) {
+  const uint32_t slot = L.x & 4095u;
+  L.x = 16u * (L.x >> 12) + (slot & 15u);
+  ring_renorm(L);
+  return slot >> 4;
+}
+__device__ __forceinline__ void ring_open(RingLane& L, const uint8_t* bs, uint32_t ring, uint64_t a, uint64_t b,
+                                          bool ok, uint32_t* status) {
+  L.ring = ring;
+  L.stage = make_uint4(0, 0, 0, 0);
+  if (!ok) {   // nothing is read from global memory for a lane with bad offsets
+    atomicOr(status, SKV_FLAG_CORRUPT);
+    L.base = bs;
+    L.p = 0; L.end = 0; L.rb = 1; L.last = 0;
+    L.x = kStateLow;
+    L.nxt = 0;
+    return;
+  }
+  const uint64_t a0 = a & ~63ull;
+  L.base = bs + a0;
+  L.p = (uint32_t)(a - a0);
+  L.end = (uint32_t)(b - a0);
+  L.last = (L.end - 1) >> 4;
+  const uint32_t first = L.p >> 4;
+  for (uint32_t k = first; k < first + 4; ++k)
+    if (k <= L.last) sts_u128(ring + (k & 3u) * 16u, ldg_stream(L.base + ((uint64_t)k << 4)));
+  L.rb = first + 4;
+  L.stage = load_block(L, L.rb);
+  L.x = (ring_word(L, L.p) << 16) | ring_word(L, L.p + 2);
+  L.p += 4;
+  L.nxt = ring_word(L, L.p);
+  if (L.x < kStateLow) atomicOr(status, SKV_FLAG_CORRUPT);
+}
+__device__ __forceinline__ void ring_close(const RingLane& L, uint32_t* status) {
+  if (L.x != kStateLow || L.p != L.end) atomicOr(status, SKV_FLAG_CORRUPT);
 }
 
 // lane offsets [a, b) of lane g, checked against the stream
@@ -318,13 +453,25 @@ __global__ void __launch_bounds__(256) k_build_tables(uint8_t* blob, uint32_t su
   reinterpret_cast<uint16_t*>(tb + SKV_TABLE_FREQ_OFF)[i] = (uint16_t)fr;
   reinterpret_cast<uint16_t*>(tb + SKV_TABLE_CUM_OFF)[i] = (uint16_t)cum;
   if (i == 255) reinterpret_cast<uint16_t*>(tb + SKV_TABLE_CUM_OFF)[256] = 4096;
-  const uint64_t mm = ((1ull << 44) + fr - 1) / fr;   // ceil(2^44 / fr)
-  uint4 enc;
+  // encoder reciprocal: the smallest shift s with m = ceil(2^(32+s)/fr) < 2^33
+  // such that floor(x m / 2^(32+s)) = floor(x / fr) for all x < fr 2^20
+  // (error term (fr 2^20 - 1)(m fr - 2^(32+s)) < 2^(32+s)) and x m < 2^64
+  uint32_t sh = 12;
+  uint64_t mm = 0;
+  for (uint32_t s2 = 0; s2 <= 12; ++s2) {
+    const uint64_t k = 1ull << (32 + s2);
+    const uint64_t m2 = (k + fr - 1) / fr;
+    const uint64_t x1 = ((uint64_t)fr << 20) - 1;
+    if (m2 < (1ull << 33) && x1 * (m2 * fr - k) < k && __umul64hi(x1, m2) == 0) {
+      sh = s2;
+      mm = m2;
+      break;
+    }
+  }
+  uint2 enc;
   enc.x = (uint32_t)mm;
-  enc.y = (uint32_t)(mm >> 32);
-  enc.z = fr << 20;
-  enc.w = (4096u - fr) | (cum << 16);
-  reinterpret_cast<uint4*>(tb + SKV_TABLE_ENC_OFF)[i] = enc;
+  enc.y = (fr << 20) | (cum << 8) | ((uint32_t)(mm >> 32) << 7) | sh;
+  reinterpret_cast<uint2*>(tb + SKV_TABLE_ENC_OFF)[i] = enc;
   reinterpret_cast<uint32_t*>(tb + SKV_TABLE_DEC_OFF)[i] = fr | (cum << 16);
   __syncthreads();
   // slot -> symbol: the last symbol whose cum <= slot
@@ -437,6 +584,13 @@ struct CodecArgs {
   uint32_t* status;
   uint64_t n_chunks, cps, slice_pos, n_lanes, slot_words;
   uint32_t K, D, C;
+  // encode, KV: fused look-back placement
+  unsigned long long* chunk_state;  // per chunk: flag << 62 | bytes
+  unsigned long long* ticket;       // next chunk to hand out
+  uint64_t* lane_offsets;
+  uint8_t* out_bs;                  // final bitstream
+  uint64_t cap;
+  uint64_t slot_warps;              // warps that own a slot set in the workspace
 };
 
 template <int ESZ>
@@ -462,45 +616,190 @@ __device__ __forceinline__ void load_lane_tables(const CodecArgs& a, uint64_t sl
   if (bad) atomicOr(a.status, SKV_FLAG_BAD_BIN);
 }
 
+// Flush the oldest complete 16-byte blocks of a lane's word buffer (the top of
+// the downward-growing buffer) to its global scratch slot, downward from gp;
+// the remaining partial block moves to the top.  With all = true every block
+// goes out, the lowest one padded below the lane's first word.
+__device__ __forceinline__ void emit_flush(uint32_t buf_top, uint32_t& rp, uint8_t*& gp, bool all) {
+  const uint32_t fill = buf_top - rp;
+  const uint32_t nb = all ? (fill + 15) >> 4 : fill >> 4;
+  for (uint32_t j = 1; j <= nb; ++j) stg_u128(gp - 16 * j, lds_u128(buf_top - 16 * j));
+  gp -= 16 * nb;
+  if (!all) {
+    const uint32_t rem = fill & 15;
+    if (rem) sts_u128(buf_top - 16, lds_u128(buf_top - 16 * nb - 16));
+    rp = buf_top - rem;
+  }
+}
+
+// ---- decoupled look-back over chunks -------------------------------------
+// chunk_state[c] = flag << 62 | value: flag 1 = the chunk's byte total is
+// published, 2 = the inclusive prefix (bytes of chunks 0..c) is published,
+// 3 = a predecessor failed.  Chunks are handed out in increasing order by an
+// atomic ticket, so every chunk a warp waits on is held by a running warp.
+constexpr unsigned long long kStAgg = 1ull << 62, kStInc = 2ull << 62, kStErr = 3ull << 62;
+constexpr unsigned long long kStVal = (1ull << 62) - 1;
+constexpr uint32_t kMaxSpins = 1u << 21;   // ~1 s of polling before giving up
+
+__device__ __forceinline__ void st_release(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long warp_sum64(unsigned long long v) {
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+// Exclusive byte prefix of chunk c (whole warp calls); ~0 if it failed.
+__device__ unsigned long long chunk_lookback(unsigned long long* st, uint64_t c, unsigned long long total,
+                                             uint32_t* status) {
+  const uint32_t tid = threadIdx.x & 31;
+  if (c == 0) {
+    if (tid == 0) st_release(&st[0], kStInc | total);
+    return 0;
+  }
+  if (tid == 0) st_release(&st[c], kStAgg | total);
+  unsigned long long excl = 0;
+  long long j = (long long)c - 1;
+  uint32_t spins = 0;
+  bool failed = false;
+  while (true) {
+    const long long idx = j - (long long)tid;
+    const unsigned long long v = idx >= 0 ? ld_acquire(&st[idx]) : kStInc;
+    const uint32_t flag = (uint32_t)(v >> 62);
+    const uint32_t stop = __ballot_sync(0xFFFFFFFFu, flag >= 2);   // inclusive or failed
+    const uint32_t none = __ballot_sync(0xFFFFFFFFu, flag == 0);
+    const uint32_t upto = stop ? ((2u << (__ffs(stop) - 1)) - 1) : 0xFFFFFFFFu;   // lanes 0..first stop
+    if (none & upto) {                                              // a predecessor is still coding
+      if (++spins > kMaxSpins) { failed = true; break; }
+      __nanosleep(100);
+      continue;
+    }
+    if (stop && ((v >> 62) == 3) && tid == (uint32_t)(__ffs(stop) - 1)) failed = true;
+    failed = __any_sync(0xFFFFFFFFu, failed);
+    if (failed) break;
+    excl += warp_sum64((tid < 32 && (upto >> tid) & 1) ? (v & kStVal) : 0ull);
+    if (stop) break;
+    j -= 32;
+  }
+  if (failed) {
+    if (tid == 0) {
+      atomicOr(status, SKV_FLAG_TIMEOUT);
+      st_release(&st[c], kStErr);
+    }
+    return ~0ull;
+  }
+  if (tid == 0) st_release(&st[c], kStInc | (excl + total));
+  return excl;
+}
+
+// Warp-cooperative copy of n_w 16-bit words from src to dst (both 2-byte
+// aligned): 32-bit accesses, a 16-bit funnel when the two differ by 2 mod 4,
+// four independent loads in flight per thread.
+__device__ __forceinline__ void warp_copy_words(uint16_t* dst, const uint16_t* src, uint32_t n_w, uint32_t tid) {
+  if (n_w == 0) return;
+  if ((reinterpret_cast<uintptr_t>(dst) & 3) != 0) {   // make dst 4-byte aligned
+    if (tid == 0) dst[0] = src[0];
+    ++dst; ++src; --n_w;
+  }
+  const uint32_t n32 = n_w >> 1;
+  uint32_t* d32 = reinterpret_cast<uint32_t*>(dst);
+  if ((reinterpret_cast<uintptr_t>(src) & 3) == 0) {
+    const uint32_t* s32 = reinterpret_cast<const uint32_t*>(src);
+    for (uint32_t k0 = 0; k0 < n32; k0 += 128) {
+      uint32_t v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t k = k0 + u * 32 + tid;
+        v[u] = k < n32 ? __ldcs(s32 + k) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t k = k0 + u * 32 + tid;
+        if (k < n32) d32[k] = v[u];
+      }
+    }
+  } else {
+    const uint32_t* s32 = reinterpret_cast<const uint32_t*>(src - 1);   // aligned, one word early
+    for (uint32_t k0 = 0; k0 < n32; k0 += 128) {
+      uint32_t lo[4], hi[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t k = k0 + u * 32 + tid;
+        lo[u] = k < n32 ? __ldcs(s32 + k) : 0u;
+        hi[u] = k < n32 ? __ldcs(s32 + k + 1) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t k = k0 + u * 32 + tid;
+        if (k < n32) d32[k] = __funnelshift_r(lo[u], hi[u], 16);
+      }
+    }
+  }
+  if ((n_w & 1) && tid == 0) dst[n_w - 1] = src[n_w - 1];
+}
+
 template <int ESZ>
 __global__ void __launch_bounds__(kCodecThreads, 1) k_encode_kv(CodecArgs a) {
   constexpr int G = 16 / ESZ;
-  extern __shared__ __align__(16) uint8_t smem[];
-  // stage the 32 encoder tables
+  uint8_t* const smem = g_smem;
+  // stage the 32 encoder tables (8-byte entries)
   for (uint32_t k = threadIdx.x; k < kKvTables * 256; k += blockDim.x) {
-    const uint32_t t = k >> 8, s = k & 255;
-    *reinterpret_cast<uint4*>(smem + t * kEncSmemStride + s * 16) =
-        reinterpret_cast<const uint4*>(a.tables + (uint64_t)t * SKV_TABLE_STRIDE + SKV_TABLE_ENC_OFF)[s];
+    const uint32_t t = k >> 8, sidx = k & 255;
+    *reinterpret_cast<uint2*>(smem + t * kEncTabStride + sidx * 8) =
+        reinterpret_cast<const uint2*>(a.tables + (uint64_t)t * SKV_TABLE_STRIDE + SKV_TABLE_ENC_OFF)[sidx];
   }
   __syncthreads();
-  const uint32_t lane = threadIdx.x & 31;
-  const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
+  const uint32_t tab0 = 0;   // offsets into g_smem
+  const uint32_t tid = threadIdx.x & 31;
+  // threads take lanes so that the R lanes sharing a channel set are adjacent:
+  // a half-warp's table reads then touch at most 16/R channel sets
+  const uint32_t R = 32u * G / a.D, CS = 32u / R;
+  const uint32_t lane = (tid % R) * CS + tid / R;
+  const uint32_t owner_of_tid = (tid % CS) * R + tid / CS;    // thread coding format lane tid
+  const uint32_t buf_top = tab0 + kEncTabBytes + (threadIdx.x + 1) * kEmitBytes;
+  const uint64_t warp_gid = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (warp_gid >= a.slot_warps) return;   // the workspace holds slots for slot_warps warps only
+  uint8_t* const my_slot_end = reinterpret_cast<uint8_t*>(a.slots + (warp_gid * kLanes + tid + 1) * a.slot_words);
   const uint64_t chunk_pos = (uint64_t)kLanes * a.K;
-  for (uint64_t chunk = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); chunk < a.n_chunks;
-       chunk += warps) {
+  while (true) {
+    unsigned long long chunk = 0;
+    if (tid == 0) chunk = atomicAdd(a.ticket, 1ull);
+    chunk = __shfl_sync(0xFFFFFFFFu, chunk, 0);
+    if (chunk >= a.n_chunks) break;
     const uint64_t slice = chunk / a.cps;
     const uint64_t first = (chunk - slice * a.cps) * chunk_pos;
     const uint64_t n_pos = min(chunk_pos, a.slice_pos - first);
     const uint32_t n_groups = (uint32_t)(n_pos / G);
     const uint32_t n_g = lane < n_groups ? (n_groups - lane + 31) / 32 : 0;
+    const int n_iter = (int)((n_groups + 31) / 32);            // warp-uniform (lane 0 has the most)
     uint32_t tb[G];
-    load_lane_tables<ESZ>(a, slice, (lane * G) % a.D, kEncSmemStride, tb);
-    const uint8_t* tg = a.tgt + (slice * a.slice_pos + first) * ESZ + lane * 16;
-    const uint8_t* pd = a.prd + (slice * a.slice_pos + first) * ESZ + lane * 16;
-    const uint64_t g = chunk * kLanes + lane;
-    uint16_t* const slot_end = a.slots + (g + 1) * a.slot_words;
-    uint16_t* wp = slot_end;
+    load_lane_tables<ESZ>(a, slice, (lane * G) % a.D, kEncTabStride, tb);
+#pragma unroll
+    for (int e = 0; e < G; ++e) tb[e] += tab0;
+    const uint64_t off = (slice * a.slice_pos + first) * ESZ + lane * 16;
+    uint8_t* gp = my_slot_end;
+    uint32_t rp = buf_top;
     uint32_t x = kStateLow;
     uint4 tc = make_uint4(0, 0, 0, 0), pc = tc;
     if (n_g) {
-      tc = ldg_stream(tg + (uint64_t)(n_g - 1) * 512);
-      pc = ldg_stream(pd + (uint64_t)(n_g - 1) * 512);
+      tc = ldg_stream(a.tgt + off + (uint64_t)(n_g - 1) * 512);
+      pc = ldg_stream(a.prd + off + (uint64_t)(n_g - 1) * 512);
     }
-    for (int i = (int)n_g - 1; i >= 0; --i) {
+    for (int i = n_iter - 1; i >= 0; --i) {
+      if (__any_sync(0xFFFFFFFFu, buf_top - rp >= kEmitFlush)) {
+        if (buf_top - rp >= kEmitFlush) emit_flush(buf_top, rp, gp, false);
+      }
+      const uint32_t act = __ballot_sync(0xFFFFFFFFu, i < (int)n_g);
+      if (i >= (int)n_g) continue;
       uint4 tn = tc, pn = pc;
       if (i > 0) {
-        tn = ldg_stream(tg + (uint64_t)(i - 1) * 512);
-        pn = ldg_stream(pd + (uint64_t)(i - 1) * 512);
+        tn = ldg_stream(a.tgt + off + (uint64_t)(i - 1) * 512);
+        pn = ldg_stream(a.prd + off + (uint64_t)(i - 1) * 512);
       }
       uint32_t tw[4], pw[4];
 #pragma unroll
@@ -515,41 +814,80 @@ __global__ void __launch_bounds__(kCodecThreads, 1) k_encode_kv(CodecArgs a) {
         const int wi = ESZ == 1 ? (e >> 2) : (e >> 1);
         const int r = (int)((tw[wi] >> sh) & mk) - (int)((pw[wi] >> sh) & mk);
         uint32_t sym = (uint32_t)(r + 127);
-        if (sym > 254u) {
-          const uint32_t raw = (uint32_t)r & mk;
-          enc_raw(x, wp, raw & 0xFFu);
-          if (ESZ == 2) enc_raw(x, wp, raw >> 8);
-          sym = 255;
+        // escapes are rare: a warp-uniform test keeps their steps off the common path
+        if (__any_sync(act, sym > 254u)) {
+          if (sym > 254u) {
+            const uint32_t raw = (uint32_t)r & mk;
+            enc_raw_smem(x, rp, raw & 0xFFu);
+            if (ESZ == 2) enc_raw_smem(x, rp, raw >> 8);
+            sym = 255;
+          }
         }
-        const uint4 en = *reinterpret_cast<const uint4*>(smem + tb[e] + sym * 16);
-        enc_step(x, wp, en);
+        enc_step_smem(x, rp, lds_u64(tb[e] + sym * 8));
       }
       tc = tn;
       pc = pn;
     }
-    *--wp = (uint16_t)x;
-    *--wp = (uint16_t)(x >> 16);
-    a.lane_words[g] = (uint32_t)(slot_end - wp);
+    if (buf_top - rp >= kEmitFlush) emit_flush(buf_top, rp, gp, false);
+    rp -= 2;
+    sts_u16(rp, x & 0xFFFFu);
+    rp -= 2;
+    sts_u16(rp, x >> 16);
+    const uint32_t my_bytes = (uint32_t)(my_slot_end - gp) + (buf_top - rp);
+    emit_flush(buf_top, rp, gp, true);
+    // lane lengths in format-lane order, chunk total, place the chunk
+    const uint32_t len = __shfl_sync(0xFFFFFFFFu, my_bytes, owner_of_tid);
+    uint32_t incl = len;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (tid >= (uint32_t)o) incl += u;
+    }
+    const unsigned long long total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    // pull this thread's own lane stream toward L2 while the look-back polls
+    for (uint32_t o = 0; o < my_bytes; o += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(my_slot_end - my_bytes + o));
+    const unsigned long long excl = chunk_lookback(a.chunk_state, chunk, total, a.status);
+    if (excl == ~0ull) continue;
+    const unsigned long long lane_off = excl + incl - len;
+    a.lane_offsets[chunk * kLanes + tid] = lane_off;
+    if (chunk + 1 == a.n_chunks && tid == 31) a.lane_offsets[a.n_lanes] = excl + total;
+    if (excl + total > a.cap) {
+      if (tid == 0) atomicOr(a.status, SKV_FLAG_CAPACITY);
+      continue;
+    }
+    __syncwarp();
+    // copy the 32 lane streams (contiguous in the output) from the slots
+    for (uint32_t l = 0; l < kLanes; ++l) {
+      const uint32_t n_w = __shfl_sync(0xFFFFFFFFu, len, l) >> 1;
+      const unsigned long long dst = __shfl_sync(0xFFFFFFFFu, lane_off, l);
+      const uint32_t owner = (l % CS) * R + l / CS;
+      const uint16_t* src = reinterpret_cast<const uint16_t*>(
+          reinterpret_cast<const uint8_t*>(a.slots + (warp_gid * kLanes + owner + 1) * a.slot_words)) - n_w;
+      warp_copy_words(reinterpret_cast<uint16_t*>(a.out_bs + dst), src, n_w, tid);
+    }
+    __syncwarp();
   }
 }
 
 // ---------------------------------------------------------------------------
-// Decoder, KV caches, fused with reconstruction.
+// Decoder, KV caches, fused with reconstruction.  Each lane reads its words
+// through a shared-memory ring (refilled every SUB symbols), looks the slot
+// up in the shared slot->symbol table, rebuilds the target from the
+// prediction's ordinal and stores whole 16-byte groups.
 // ---------------------------------------------------------------------------
 template <int ESZ>
 __global__ void __launch_bounds__(kCodecThreads, 1) k_decode_kv(CodecArgs a) {
   constexpr int G = 16 / ESZ;
-  extern __shared__ __align__(16) uint8_t smem[];
-  // stage LUT (4096 B) + decoder entries (1024 B) of the 32 tables
-  for (uint32_t k = threadIdx.x; k < kKvTables * 320; k += blockDim.x) {
-    const uint32_t t = k / 320, s = k % 320;
-    const uint4 v = reinterpret_cast<const uint4*>(a.tables + (uint64_t)t * SKV_TABLE_STRIDE +
-                                                   SKV_TABLE_LUT_OFF)[s];
-    uint32_t* dst = reinterpret_cast<uint32_t*>(smem + t * kDecSmemStride + s * 16);
-    dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
+  constexpr int SUB = ESZ == 1 ? 8 : 4;   // at most 32 / 24 stream bytes between refills
+  uint8_t* const smem = g_smem;
+  for (uint32_t k = threadIdx.x; k < kKvTables * 1280; k += blockDim.x) {
+    const uint32_t t = k / 1280, w = k % 1280;
+    reinterpret_cast<uint32_t*>(smem + t * kDecTabStride)[w] =
+        reinterpret_cast<const uint32_t*>(a.tables + (uint64_t)t * SKV_TABLE_STRIDE + SKV_TABLE_LUT_OFF)[w];
   }
   __syncthreads();
+  const uint32_t tab0 = 0;   // offsets into g_smem
   const uint32_t lane = threadIdx.x & 31;
+  const uint32_t ring = tab0 + kDecTabBytes + threadIdx.x * kRingBytes;
   const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
   const uint64_t chunk_pos = (uint64_t)kLanes * a.K;
   for (uint64_t chunk = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); chunk < a.n_chunks;
@@ -560,17 +898,22 @@ __global__ void __launch_bounds__(kCodecThreads, 1) k_decode_kv(CodecArgs a) {
     const uint32_t n_groups = (uint32_t)(n_pos / G);
     const uint32_t n_g = lane < n_groups ? (n_groups - lane + 31) / 32 : 0;
     uint32_t tb[G];
-    load_lane_tables<ESZ>(a, slice, (lane * G) % a.D, kDecSmemStride, tb);
+    load_lane_tables<ESZ>(a, slice, (lane * G) % a.D, kDecTabStride, tb);
+#pragma unroll
+    for (int e = 0; e < G; ++e) tb[e] += tab0;
     const uint64_t g = chunk * kLanes + lane;
     uint64_t sa, sb;
     const bool ok = lane_span(a.offs, g, a.n_lanes, a.n_bytes, &sa, &sb);
-    DecLane L;
-    dec_open(L, a.bs, sa, sb, ok, a.status);
+    RingLane L;
+    ring_open(L, a.bs, ring, sa, sb, ok, a.status);
     const uint8_t* pd = a.prd + (slice * a.slice_pos + first) * ESZ + lane * 16;
     uint8_t* od = a.out + (slice * a.slice_pos + first) * ESZ + lane * 16;
     uint4 pc = make_uint4(0, 0, 0, 0);
     if (n_g) pc = ldg_stream(pd);
-    for (uint32_t i = 0; i < n_g; ++i) {
+    const uint32_t n_iter = (n_groups + 31) / 32;              // warp-uniform
+    for (uint32_t i = 0; i < n_iter; ++i) {
+      const uint32_t act = __ballot_sync(0xFFFFFFFFu, i < n_g);
+      if (i >= n_g) continue;
       uint4 pn = pc;
       if (i + 1 < n_g) pn = ldg_stream(pd + (uint64_t)(i + 1) * 512);
       uint32_t pw[4], ow[4] = {0, 0, 0, 0};
@@ -581,17 +924,19 @@ __global__ void __launch_bounds__(kCodecThreads, 1) k_decode_kv(CodecArgs a) {
         constexpr uint32_t mk = ESZ == 1 ? 0xFFu : 0xFFFFu;
         const uint32_t sh = ESZ == 1 ? 8 * (e & 3) : 16 * (e & 1);
         const int wi = ESZ == 1 ? (e >> 2) : (e >> 1);
+        if (e % SUB == 0) ring_refill(L);
         const uint32_t slot = L.x & 4095u;
-        const uint32_t sym = smem[tb[e] + slot];
-        const uint32_t dv = *reinterpret_cast<const uint32_t*>(smem + tb[e] + 4096 + sym * 4);
+        const uint32_t sym = lds_u8(tb[e] + slot);
+        const uint32_t dv = lds_u32(tb[e] + 4096u + sym * 4u);
         L.x = (dv & 0xFFFFu) * (L.x >> 12) + slot - (dv >> 16);
-        dec_renorm(L);
-        uint32_t r;
-        if (sym == 255u) {
-          r = dec_raw(L);
-          if (ESZ == 2) r = (r << 8) | dec_raw(L);
-        } else {
-          r = sym - 127u;
+        ring_renorm(L);
+        uint32_t r = sym - 127u;
+        // escapes are rare: a warp-uniform test keeps their steps off the common path
+        if (__any_sync(act, sym == 255u)) {
+          if (sym == 255u) {
+            r = ring_raw(L);
+            if (ESZ == 2) r = (r << 8) | ring_raw(L);
+          }
         }
         const uint32_t ut = (((pw[wi] >> sh) & mk) + r) & mk;
         ow[wi] |= ut << sh;
@@ -604,7 +949,7 @@ __global__ void __launch_bounds__(kCodecThreads, 1) k_decode_kv(CodecArgs a) {
       stg_stream(od + (uint64_t)i * 512, o);
       pc = pn;
     }
-    dec_close(L, a.status);
+    ring_close(L, a.status);
   }
 }
 
@@ -654,15 +999,15 @@ __global__ void __launch_bounds__(256) k_encode_coef(CodecArgs a) {
         uint32_t sym = (uint32_t)(r + 127);
         if (sym > 254u) {
           const uint32_t raw = (uint32_t)r & 0xFFFFu;
-          enc_raw(x, wp, raw & 0xFFu);
-          enc_raw(x, wp, raw >> 8);
+          enc_raw_gmem(x, wp, raw & 0xFFu);
+          enc_raw_gmem(x, wp, raw >> 8);
           sym = 255;
         }
         uint32_t tbl = 16u * bin + f;
         if (bin > 63u) { atomicOr(a.status, SKV_FLAG_BAD_BIN); tbl = 1023; }
-        const uint4 en = __ldg(reinterpret_cast<const uint4*>(a.tables + (uint64_t)tbl * SKV_TABLE_STRIDE +
+        const uint2 en = __ldg(reinterpret_cast<const uint2*>(a.tables + (uint64_t)tbl * SKV_TABLE_STRIDE +
                                                               SKV_TABLE_ENC_OFF) + sym);
-        enc_step(x, wp, en);
+        enc_step_gmem(x, wp, en);
       }
     }
     *--wp = (uint16_t)x;
@@ -849,6 +1194,7 @@ void codec_grid(uint64_t n_chunks, int* blocks, int* threads) {
   if (warps_per_block < 1) warps_per_block = 1;
   uint64_t nb = (n_chunks + warps_per_block - 1) / warps_per_block;
   if (nb > (uint64_t)sms) nb = sms;
+  if (nb * warps_per_block > kMaxWarps) nb = kMaxWarps / warps_per_block;
   *blocks = (int)(nb < 1 ? 1 : nb);
   *threads = (int)(warps_per_block * 32);
 }
@@ -997,20 +1343,41 @@ int skv_encode(const skv_params* p, const void* d_target, const void* d_pred, co
   st = cuda_status(cudaMemsetAsync(d_status, 0, 4, s));
   if (st != SKV_OK) return st;
   int blocks, threads;
-  if (g.dtype == SKV_COEF_I16) {
+  if (g.dtype != SKV_COEF_I16) {
+    // one kernel: lanes coded into per-warp slots, chunks placed by look-back
+    a.chunk_state = reinterpret_cast<unsigned long long*>(ws + wl.state_off);
+    a.ticket = reinterpret_cast<unsigned long long*>(ws + wl.ticket_off);
+    a.lane_offsets = d_lane_offsets;
+    a.out_bs = static_cast<uint8_t*>(d_bitstream);
+    a.cap = cap_bytes;
+    a.slot_warps = wl.n_slots / kLanes;
+    st = cuda_status(cudaMemsetAsync(ws + wl.state_off, 0, wl.total - wl.state_off, s));
+    if (st != SKV_OK) return st;
+    codec_grid(g.n_chunks, &blocks, &threads);
+    const int smem_bytes = (int)(kEncTabBytes + (uint32_t)threads * kEmitBytes);
+    if (g.esz == 1) {
+      if ((st = set_smem(k_encode_kv<1>, kEncTabBytes + kCodecThreads * kEmitBytes)) != SKV_OK) return st;
+      k_encode_kv<1><<<blocks, threads, smem_bytes, s>>>(a);
+    } else {
+      if ((st = set_smem(k_encode_kv<2>, kEncTabBytes + kCodecThreads * kEmitBytes)) != SKV_OK) return st;
+      k_encode_kv<2><<<blocks, threads, smem_bytes, s>>>(a);
+    }
+    if ((st = launch_check()) != SKV_OK) return st;
+    if (h_total_bytes) {
+      uint64_t total = 0;
+      st = cuda_status(cudaMemcpyAsync(&total, d_lane_offsets + g.n_lanes, 8, cudaMemcpyDeviceToHost, s));
+      if (st == SKV_OK) st = cuda_status(cudaStreamSynchronize(s));
+      if (st != SKV_OK) return st;
+      *h_total_bytes = total;
+      if (total > cap_bytes) return SKV_ERR_CAPACITY;
+    }
+    return SKV_OK;
+  }
+  {
     int sms = sm_count();
     uint64_t nb = (g.n_chunks + 7) / 8;
     uint64_t cap_blocks = (uint64_t)(sms > 0 ? sms : 1) * 8;
     k_encode_coef<<<(unsigned)(nb < cap_blocks ? nb : cap_blocks), 256, 0, s>>>(a);
-  } else {
-    codec_grid(g.n_chunks, &blocks, &threads);
-    if (g.esz == 1) {
-      if ((st = set_smem(k_encode_kv<1>, kEncSmemBytes)) != SKV_OK) return st;
-      k_encode_kv<1><<<blocks, threads, kEncSmemBytes, s>>>(a);
-    } else {
-      if ((st = set_smem(k_encode_kv<2>, kEncSmemBytes)) != SKV_OK) return st;
-      k_encode_kv<2><<<blocks, threads, kEncSmemBytes, s>>>(a);
-    }
   }
   if ((st = launch_check()) != SKV_OK) return st;
   unsigned long long* part = reinterpret_cast<unsigned long long*>(ws + wl.part_off);
@@ -1049,7 +1416,7 @@ int skv_decode(const skv_params* p, const void* d_bitstream, uint64_t n_bytes, c
   if (st != SKV_OK || g.n_lanes == 0) return st;
   if (!d_bitstream || !d_lane_offsets || !d_pred || !d_tables || !d_bins || !d_target_out)
     return SKV_ERR_INVALID_ARG;
-  if (((uintptr_t)d_bitstream & 1) || ((uintptr_t)d_lane_offsets & 7) || !aligned16(d_pred) ||
+  if (!aligned16(d_bitstream) || ((uintptr_t)d_lane_offsets & 7) || !aligned16(d_pred) ||
       !aligned16(d_tables) || !aligned16(d_bins) || !aligned16(d_target_out))
     return SKV_ERR_INVALID_ARG;
   CodecArgs a;
@@ -1078,12 +1445,13 @@ int skv_decode(const skv_params* p, const void* d_bitstream, uint64_t n_bytes, c
   }
   int blocks, threads;
   codec_grid(g.n_chunks, &blocks, &threads);
+  const int smem_bytes = (int)(kDecTabBytes + (uint32_t)threads * kRingBytes);
   if (g.esz == 1) {
-    if ((st = set_smem(k_decode_kv<1>, kDecSmemBytes)) != SKV_OK) return st;
-    k_decode_kv<1><<<blocks, threads, kDecSmemBytes, s>>>(a);
+    if ((st = set_smem(k_decode_kv<1>, kDecTabBytes + kCodecThreads * kRingBytes)) != SKV_OK) return st;
+    k_decode_kv<1><<<blocks, threads, smem_bytes, s>>>(a);
   } else {
-    if ((st = set_smem(k_decode_kv<2>, kDecSmemBytes)) != SKV_OK) return st;
-    k_decode_kv<2><<<blocks, threads, kDecSmemBytes, s>>>(a);
+    if ((st = set_smem(k_decode_kv<2>, kDecTabBytes + kCodecThreads * kRingBytes)) != SKV_OK) return st;
+    k_decode_kv<2><<<blocks, threads, smem_bytes, s>>>(a);
   }
   return launch_check();
 }

@@ -19,9 +19,9 @@ HEADER = os.path.join(ROOT, "include", "skv.h")
 SKV_OK, SKV_ERR_INVALID_ARG, SKV_ERR_CUDA, SKV_ERR_CAPACITY = 0, 1, 2, 3
 SKV_ERR_CORRUPT, SKV_ERR_TIMEOUT, SKV_ERR_UNSUPPORTED = 4, 5, 6
 SKV_FP8_E4M3, SKV_BF16, SKV_COEF_I16 = 1, 2, 3
-SKV_TABLE_STRIDE = 12288
-SKV_TABLE_ENC_OFF, SKV_TABLE_LUT_OFF, SKV_TABLE_DEC_OFF = 0, 4096, 8192
-SKV_TABLE_FREQ_OFF, SKV_TABLE_CUM_OFF = 9216, 9728
+SKV_TABLE_STRIDE = 8704
+SKV_TABLE_ENC_OFF, SKV_TABLE_LUT_OFF, SKV_TABLE_DEC_OFF = 0, 2048, 6144
+SKV_TABLE_FREQ_OFF, SKV_TABLE_CUM_OFF = 7168, 7680
 
 
 class SkvError(RuntimeError):

@@ -135,15 +135,18 @@ def test_table_blob_structures(nat, kind):
     for t in range(blob.shape[0]):
         f = fr[t].astype(np.int64)
         c = cum[t].astype(np.int64)
-        enc = blob[t, nat.SKV_TABLE_ENC_OFF:nat.SKV_TABLE_ENC_OFF + 4096].copy().view(np.uint32).reshape(256, 4)
-        m = enc[:, 0].astype(object) + (enc[:, 1].astype(object) << 32)
+        enc = blob[t, nat.SKV_TABLE_ENC_OFF:nat.SKV_TABLE_ENC_OFF + 2048].copy().view(np.uint32).reshape(256, 2)
         for i in range(256):
             fi = int(f[i])
-            assert m[i] == -(-(1 << 44) // fi)
-            # floor(x/fr) = floor(x m / 2^44) for all x < fr 2^20: error term (fr 2^20 - 1)(m fr - 2^44) < 2^44
-            assert (fi * (1 << 20) - 1) * (m[i] * fi - (1 << 44)) < (1 << 44)
-        assert np.array_equal(enc[:, 2], (f << 20).astype(np.uint32))
-        assert np.array_equal(enc[:, 3], ((4096 - f) | (c[:256] << 16)).astype(np.uint32))
+            w = int(enc[i, 1])
+            sh, h = w & 31, (w >> 7) & 1
+            assert w >> 20 == fi and (w >> 8) & 0xFFF == int(c[i]) and (w >> 5) & 3 == 0
+            k = 1 << (32 + sh)
+            m = (h << 32) | int(enc[i, 0])
+            assert m == -(-k // fi)
+            # floor(x/fr) = floor(x m / 2^(32+s)) for every x < fr 2^20 and x m < 2^64
+            x1 = fi * (1 << 20) - 1
+            assert x1 * (m * fi - k) < k and x1 * m < (1 << 64)
         dec = blob[t, nat.SKV_TABLE_DEC_OFF:nat.SKV_TABLE_DEC_OFF + 1024].copy().view(np.uint32)
         assert np.array_equal(dec, (f | (c[:256] << 16)).astype(np.uint32))
         lut = blob[t, nat.SKV_TABLE_LUT_OFF:nat.SKV_TABLE_LUT_OFF + 4096]
