@@ -60,7 +60,11 @@ constexpr uint32_t kRingBytes = 64;                                // per-lane s
 #ifndef SKV_CODEC_THREADS
 #define SKV_CODEC_THREADS 1024
 #endif
-constexpr int kCodecThreads = SKV_CODEC_THREADS;   // threads per codec CTA (one CTA per SM)
+constexpr int kCodecThreads = SKV_CODEC_THREADS;   // decoder threads per CTA (one CTA per SM)
+#ifndef SKV_ENC_THREADS
+#define SKV_ENC_THREADS 1024
+#endif
+constexpr int kEncThreads = SKV_ENC_THREADS;       // encoder threads per CTA (more registers per thread)
 constexpr int kScanPerBlock = 4096;       // lanes per scan block (256 threads x 16)
 
 // ---------------------------------------------------------------------------
@@ -163,20 +167,24 @@ int sm_count() {
 // Device helpers
 // ---------------------------------------------------------------------------
 
-// ordinals of four FP8 patterns at once: non-negative b -> b | 0x80, negative
-// b -> ~b; the inverse flips with the complementary mask
-__device__ __forceinline__ uint32_t ord8x4(uint32_t w) {
-  return w ^ (((w >> 7) & 0x01010101u) * 0x7Fu | 0x80808080u);
+// Ordinals of four FP8 (two BF16) patterns at once: non-negative b -> b | top,
+// negative b -> ~b.  prmt with selector nibbles 8..15 replicates the sign bit
+// of a byte over the target byte, giving the per-lane mask in one instruction;
+// the inverse takes the sign from the complemented ordinal.
+__device__ __forceinline__ uint32_t sign_bytes8(uint32_t w) {
+  uint32_t m;
+  asm("prmt.b32 %0, %1, 0, 0xBA98;" : "=r"(m) : "r"(w));
+  return m;
 }
-__device__ __forceinline__ uint32_t unord8x4(uint32_t u) {
-  return u ^ (((~u >> 7) & 0x01010101u) * 0x7Fu | 0x80808080u);
+__device__ __forceinline__ uint32_t sign_halves16(uint32_t w) {
+  uint32_t m;
+  asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(m) : "r"(w));
+  return m;
 }
-__device__ __forceinline__ uint32_t ord16x2(uint32_t w) {
-  return w ^ (((w >> 15) & 0x00010001u) * 0x7FFFu | 0x80008000u);
-}
-__device__ __forceinline__ uint32_t unord16x2(uint32_t u) {
-  return u ^ (((~u >> 15) & 0x00010001u) * 0x7FFFu | 0x80008000u);
-}
+__device__ __forceinline__ uint32_t ord8x4(uint32_t w) { return w ^ (sign_bytes8(w) | 0x80808080u); }
+__device__ __forceinline__ uint32_t unord8x4(uint32_t u) { return u ^ (sign_bytes8(~u) | 0x80808080u); }
+__device__ __forceinline__ uint32_t ord16x2(uint32_t w) { return w ^ (sign_halves16(w) | 0x80008000u); }
+__device__ __forceinline__ uint32_t unord16x2(uint32_t u) { return u ^ (sign_halves16(~u) | 0x80008000u); }
 
 // streaming (evict-first) 128-bit loads and stores of the caches
 __device__ __forceinline__ uint4 ldg_stream(const void* ptr) { return __ldcs(reinterpret_cast<const uint4*>(ptr)); }
@@ -232,14 +240,16 @@ __device__ __forceinline__ void enc_step_smem(uint32_t& x, uint32_t& rp, uint2 e
   const uint32_t q = enc_quot(x, e.x, e.y);
   x = x + q * (4096u - (e.y >> 20)) + ((e.y >> 8) & 0xFFFu);
 }
-// raw byte v as a uniform step (fr 16, cum 16 v)
-__device__ __forceinline__ void enc_raw_smem(uint32_t& x, uint32_t& rp, uint32_t v) {
-  if (x >= (1u << 24)) {
+// raw byte v as a uniform step (fr 16, cum 16 v), taken only where do_it holds
+__device__ __forceinline__ void enc_raw_smem_if(uint32_t& x, uint32_t& rp, uint32_t v, bool do_it) {
+  const bool ren = do_it && x >= (1u << 24);
+  if (ren) {
     rp -= 2;
     sts_u16(rp, x);
-    x >>= 16;
   }
-  x = ((x >> 4) << 12) | (x & 15u) | (v << 4);
+  const uint32_t xr = ren ? x >> 16 : x;
+  const uint32_t xn = ((xr >> 4) << 12) | (xr & 15u) | (v << 4);
+  x = do_it ? xn : x;
 }
 // the same with words written downward straight into global scratch (COEF path)
 __device__ __forceinline__ void enc_step_gmem(uint32_t& x, uint16_t*& wp, uint2 e) {
@@ -312,17 +322,22 @@ struct RingLane {
 __device__ __forceinline__ uint4 load_block(const RingLane& L, uint32_t k) {
   return k <= L.last ? ldg_stream(L.base + ((uint64_t)k << 4)) : make_uint4(0, 0, 0, 0);
 }
-// make blocks [p/16, p/16 + 4) resident
-__device__ __forceinline__ void ring_refill(RingLane& L) {
-  const uint32_t need = (L.p >> 4) + 4;
-  while (L.rb < need) {
-    sts_u128(L.ring + (L.rb & 3u) * 16u, L.stage);
-    ++L.rb;
-    L.stage = load_block(L, L.rb);
+// make blocks [p/16, p/16 + 4) resident: one straight-line step covers a lane
+// that moved into a new block since the last refill; lanes that moved further
+// (escape-heavy stretches) catch up in a warp-uniform loop
+__device__ __forceinline__ void ring_step(RingLane& L) {
+  sts_u128(L.ring + (L.rb & 3u) * 16u, L.stage);
+  ++L.rb;
+  L.stage = load_block(L, L.rb);
+}
+__device__ __forceinline__ void ring_refill(RingLane& L, uint32_t act) {
+  if (L.rb < (L.p >> 4) + 4) ring_step(L);
+  while (__any_sync(act, L.rb < (L.p >> 4) + 4)) {
+    if (L.rb < (L.p >> 4) + 4) ring_step(L);
   }
 }
 __device__ __forceinline__ uint32_t ring_word(const RingLane& L, uint32_t p) {
-  return lds_u16(L.ring + (p & 63u));
+  return lds_u16((p & 63u) | L.ring);   // ring is 64-byte aligned
 }
 __device__ __forceinline__ void ring_renorm(RingLane& L) {
   if (L.x < kStateLow) {
@@ -331,10 +346,17 @@ __device__ __forceinline__ void ring_renorm(RingLane& L) {
     L.nxt = ring_word(L, L.p);
   }
 }
-__device__ __forceinline__ uint32_t ring_raw(RingLane& L) {
+// a raw byte (uniform step, fr 16) taken only where do_it holds
+__device__ __forceinline__ uint32_t ring_raw_if(RingLane& L, bool do_it) {
   const uint32_t slot = L.x & 4095u;
-  L.x = 16u * (L.x >> 12) + (slot & 15u);
-  ring_renorm(L);
+  const uint32_t xn = 16u * (L.x >> 12) + (slot & 15u);
+  const bool ren = do_it && xn < kStateLow;
+  const uint32_t pn = L.p + 2;
+  L.x = do_it ? (ren ? ((xn << 16) | L.nxt) : xn) : L.x;
+  if (ren) {
+    L.p = pn;
+    L.nxt = ring_word(L, pn);
+  }
   return slot >> 4;
 }
 __device__ __forceinline__ void ring_open(RingLane& L, const uint8_t* bs, uint32_t ring, uint64_t a, uint64_t b,
@@ -342,7 +364,7 @@ __device__ __forceinline__ void ring_open(RingLane& L, const uint8_t* bs, uint32
   L.ring = ring;
   L.stage = make_uint4(0, 0, 0, 0);
   if (!ok) {   // nothing is read from global memory for a lane with bad offsets
-    atomicOr(status, SKV_FLAG_CORRUPT);
+    if (status) atomicOr(status, SKV_FLAG_CORRUPT);   // NULL: an idle lane, not an error
     L.base = bs;
     L.p = 0; L.end = 0; L.rb = 1; L.last = 0;
     L.x = kStateLow;
@@ -362,7 +384,7 @@ __device__ __forceinline__ void ring_open(RingLane& L, const uint8_t* bs, uint32
   L.x = (ring_word(L, L.p) << 16) | ring_word(L, L.p + 2);
   L.p += 4;
   L.nxt = ring_word(L, L.p);
-  if (L.x < kStateLow) atomicOr(status, SKV_FLAG_CORRUPT);
+  if (L.x < kStateLow && status) atomicOr(status, SKV_FLAG_CORRUPT);
 }
 __device__ __forceinline__ void ring_close(const RingLane& L, uint32_t* status) {
   if (L.x != kStateLow || L.p != L.end) atomicOr(status, SKV_FLAG_CORRUPT);
@@ -744,7 +766,7 @@ __device__ __forceinline__ void warp_copy_words(uint16_t* dst, const uint16_t* s
 }
 
 template <int ESZ>
-__global__ void __launch_bounds__(kCodecThreads, 1) k_encode_kv(CodecArgs a) {
+__global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
   constexpr int G = 16 / ESZ;
   uint8_t* const smem = g_smem;
   // stage the 32 encoder tables (8-byte entries)
@@ -807,23 +829,36 @@ __global__ void __launch_bounds__(kCodecThreads, 1) k_encode_kv(CodecArgs a) {
         tw[k] = ESZ == 1 ? ord8x4(word_of(tc, k)) : ord16x2(word_of(tc, k));
         pw[k] = ESZ == 1 ? ord8x4(word_of(pc, k)) : ord16x2(word_of(pc, k));
       }
+      // blocks of 4 positions, highest first: symbols of the block up front and
+      // one warp-uniform test for escapes (rare) per block
 #pragma unroll
-      for (int e = G - 1; e >= 0; --e) {
+      for (int blk = G / 4 - 1; blk >= 0; --blk) {
         constexpr uint32_t mk = ESZ == 1 ? 0xFFu : 0xFFFFu;
-        const uint32_t sh = ESZ == 1 ? 8 * (e & 3) : 16 * (e & 1);
-        const int wi = ESZ == 1 ? (e >> 2) : (e >> 1);
-        const int r = (int)((tw[wi] >> sh) & mk) - (int)((pw[wi] >> sh) & mk);
-        uint32_t sym = (uint32_t)(r + 127);
-        // escapes are rare: a warp-uniform test keeps their steps off the common path
-        if (__any_sync(act, sym > 254u)) {
-          if (sym > 254u) {
-            const uint32_t raw = (uint32_t)r & mk;
-            enc_raw_smem(x, rp, raw & 0xFFu);
-            if (ESZ == 2) enc_raw_smem(x, rp, raw >> 8);
-            sym = 255;
-          }
+        int rr[4];
+        uint32_t sy[4];
+        bool esc = false;
+#pragma unroll
+        for (int j = 3; j >= 0; --j) {
+          const int e = blk * 4 + j;
+          const uint32_t sh = ESZ == 1 ? 8 * (e & 3) : 16 * (e & 1);
+          const int wi = ESZ == 1 ? (e >> 2) : (e >> 1);
+          rr[j] = (int)((tw[wi] >> sh) & mk) - (int)((pw[wi] >> sh) & mk);
+          sy[j] = (uint32_t)(rr[j] + 127);
+          esc |= sy[j] > 254u;
         }
-        enc_step_smem(x, rp, lds_u64(tb[e] + sym * 8));
+        if (__any_sync(act, esc)) {
+#pragma unroll
+          for (int j = 3; j >= 0; --j) {
+            const bool e_j = sy[j] > 254u;
+            const uint32_t raw = (uint32_t)rr[j] & mk;
+            enc_raw_smem_if(x, rp, raw & 0xFFu, e_j);
+            if (ESZ == 2) enc_raw_smem_if(x, rp, raw >> 8, e_j);
+            enc_step_smem(x, rp, lds_u64(tb[blk * 4 + j] + (e_j ? 255u : sy[j]) * 8));
+          }
+        } else {
+#pragma unroll
+          for (int j = 3; j >= 0; --j) enc_step_smem(x, rp, lds_u64(tb[blk * 4 + j] + sy[j] * 8));
+        }
       }
       tc = tn;
       pc = pn;
@@ -924,19 +959,20 @@ __global__ void __launch_bounds__(kCodecThreads, 1) k_decode_kv(CodecArgs a) {
         constexpr uint32_t mk = ESZ == 1 ? 0xFFu : 0xFFFFu;
         const uint32_t sh = ESZ == 1 ? 8 * (e & 3) : 16 * (e & 1);
         const int wi = ESZ == 1 ? (e >> 2) : (e >> 1);
-        if (e % SUB == 0) ring_refill(L);
+        if (e % SUB == 0) ring_refill(L, act);
         const uint32_t slot = L.x & 4095u;
         const uint32_t sym = lds_u8(tb[e] + slot);
         const uint32_t dv = lds_u32(tb[e] + 4096u + sym * 4u);
         L.x = (dv & 0xFFFFu) * (L.x >> 12) + slot - (dv >> 16);
         ring_renorm(L);
         uint32_t r = sym - 127u;
-        // escapes are rare: a warp-uniform test keeps their steps off the common path
+        // escapes are rare: a warp-uniform test keeps their steps off the common
+        // path; inside, the raw steps are predicated per lane (no nested branch)
         if (__any_sync(act, sym == 255u)) {
-          if (sym == 255u) {
-            r = ring_raw(L);
-            if (ESZ == 2) r = (r << 8) | ring_raw(L);
-          }
+          const bool esc = sym == 255u;
+          uint32_t v = ring_raw_if(L, esc);
+          if (ESZ == 2) v = (v << 8) | ring_raw_if(L, esc);
+          r = esc ? v : r;
         }
         const uint32_t ut = (((pw[wi] >> sh) & mk) + r) & mk;
         ow[wi] |= ut << sh;
@@ -1186,11 +1222,11 @@ int set_smem(Kern k, int bytes) {
 
 // blocks for a persistent codec kernel: one CTA per SM, warps spread so that
 // every SM gets work when there are few chunks
-void codec_grid(uint64_t n_chunks, int* blocks, int* threads) {
+void codec_grid(uint64_t n_chunks, int* blocks, int* threads, int max_threads) {
   int sms = sm_count();
   if (sms <= 0) sms = 1;
   uint64_t warps_per_block = (n_chunks + sms - 1) / sms;
-  if (warps_per_block > kCodecThreads / 32) warps_per_block = kCodecThreads / 32;
+  if (warps_per_block > (uint64_t)max_threads / 32) warps_per_block = max_threads / 32;
   if (warps_per_block < 1) warps_per_block = 1;
   uint64_t nb = (n_chunks + warps_per_block - 1) / warps_per_block;
   if (nb > (uint64_t)sms) nb = sms;
@@ -1353,13 +1389,13 @@ int skv_encode(const skv_params* p, const void* d_target, const void* d_pred, co
     a.slot_warps = wl.n_slots / kLanes;
     st = cuda_status(cudaMemsetAsync(ws + wl.state_off, 0, wl.total - wl.state_off, s));
     if (st != SKV_OK) return st;
-    codec_grid(g.n_chunks, &blocks, &threads);
+    codec_grid(g.n_chunks, &blocks, &threads, kEncThreads);
     const int smem_bytes = (int)(kEncTabBytes + (uint32_t)threads * kEmitBytes);
     if (g.esz == 1) {
-      if ((st = set_smem(k_encode_kv<1>, kEncTabBytes + kCodecThreads * kEmitBytes)) != SKV_OK) return st;
+      if ((st = set_smem(k_encode_kv<1>, kEncTabBytes + kEncThreads * kEmitBytes)) != SKV_OK) return st;
       k_encode_kv<1><<<blocks, threads, smem_bytes, s>>>(a);
     } else {
-      if ((st = set_smem(k_encode_kv<2>, kEncTabBytes + kCodecThreads * kEmitBytes)) != SKV_OK) return st;
+      if ((st = set_smem(k_encode_kv<2>, kEncTabBytes + kEncThreads * kEmitBytes)) != SKV_OK) return st;
       k_encode_kv<2><<<blocks, threads, smem_bytes, s>>>(a);
     }
     if ((st = launch_check()) != SKV_OK) return st;
@@ -1444,7 +1480,7 @@ int skv_decode(const skv_params* p, const void* d_bitstream, uint64_t n_bytes, c
     return launch_check();
   }
   int blocks, threads;
-  codec_grid(g.n_chunks, &blocks, &threads);
+  codec_grid(g.n_chunks, &blocks, &threads, kCodecThreads);
   const int smem_bytes = (int)(kDecTabBytes + (uint32_t)threads * kRingBytes);
   if (g.esz == 1) {
     if ((st = set_smem(k_decode_kv<1>, kDecTabBytes + kCodecThreads * kRingBytes)) != SKV_OK) return st;
