@@ -207,6 +207,17 @@ int skv_encode_noalloc(const skv_params* p, const void* d_target, const void* d_
                        uint64_t cap_bytes, uint64_t* d_lane_offsets, uint32_t* d_status,
                        uint64_t* h_total_bytes, void* stream);
 
+/* Self-test of the encoder's bounded wait (no counterpart on the pages): runs
+ * the encoder's chunk look-back for chunks 0..n_chunks-1 (chunk w has w + 1
+ * bytes) on d_state[n_chunks] (u64, cleared by the call), except that chunk
+ * missing_chunk never publishes.  Chunks before it receive their exclusive
+ * prefix in d_excl[w]; the chunk after it must give up after max_spins polls
+ * (about 100 ns each), set SKV_FLAG_TIMEOUT in d_status and mark itself
+ * failed, and every later chunk must fail at once (d_excl = ~0).  At most 4096
+ * chunks (all resident); nothing waits without a limit. */
+int skv_selftest_lookback(uint64_t* d_state, uint32_t n_chunks, uint32_t missing_chunk,
+                          uint32_t max_spins, uint64_t* d_excl, uint32_t* d_status, void* stream);
+
 /* Synchronises the stream, reads the status word and returns SKV_OK or the
  * code of the most serious flag (CORRUPT > CAPACITY > TIMEOUT > INVALID_ARG
  * for an out-of-range bin). */

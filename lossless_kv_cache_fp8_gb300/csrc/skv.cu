@@ -678,7 +678,7 @@ __device__ __forceinline__ unsigned long long warp_sum64(unsigned long long v) {
 
 // Exclusive byte prefix of chunk c (whole warp calls); ~0 if it failed.
 __device__ unsigned long long chunk_lookback(unsigned long long* st, uint64_t c, unsigned long long total,
-                                             uint32_t* status) {
+                                             uint32_t* status, uint32_t max_spins) {
   const uint32_t tid = threadIdx.x & 31;
   if (c == 0) {
     if (tid == 0) st_release(&st[0], kStInc | total);
@@ -697,7 +697,7 @@ __device__ unsigned long long chunk_lookback(unsigned long long* st, uint64_t c,
     const uint32_t none = __ballot_sync(0xFFFFFFFFu, flag == 0);
     const uint32_t upto = stop ? ((2u << (__ffs(stop) - 1)) - 1) : 0xFFFFFFFFu;   // lanes 0..first stop
     if (none & upto) {                                              // a predecessor is still coding
-      if (++spins > kMaxSpins) { failed = true; break; }
+      if (++spins > max_spins) { failed = true; break; }
       __nanosleep(100);
       continue;
     }
@@ -880,7 +880,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
     const unsigned long long total = __shfl_sync(0xFFFFFFFFu, incl, 31);
     // pull this thread's own lane stream toward L2 while the look-back polls
     for (uint32_t o = 0; o < my_bytes; o += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(my_slot_end - my_bytes + o));
-    const unsigned long long excl = chunk_lookback(a.chunk_state, chunk, total, a.status);
+    const unsigned long long excl = chunk_lookback(a.chunk_state, chunk, total, a.status, kMaxSpins);
     if (excl == ~0ull) continue;
     const unsigned long long lane_off = excl + incl - len;
     a.lane_offsets[chunk * kLanes + tid] = lane_off;
@@ -901,6 +901,17 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
     }
     __syncwarp();
   }
+}
+
+// Self-test of the encoder's bounded wait: warp w plays chunk w (total w + 1
+// bytes) through chunk_lookback; chunk `missing` never publishes, so its
+// successors must give up after max_spins polls and report a timeout.
+__global__ void k_selftest_lookback(unsigned long long* st, uint32_t n, uint32_t missing, uint32_t max_spins,
+                                    uint32_t* status, unsigned long long* excl_out) {
+  const uint32_t w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (w >= n || w == missing) return;
+  const unsigned long long e = chunk_lookback(st, w, w + 1, status, max_spins);
+  if ((threadIdx.x & 31) == 0) excl_out[w] = e;
 }
 
 // ---------------------------------------------------------------------------
@@ -1525,6 +1536,22 @@ int skv_encode_noalloc(const skv_params* p, const void* d_target, const void* d_
   }
   return skv_encode(p, d_target, d_pred, d_tables, d_bins, d_bitstream, cap_bytes, d_lane_offsets, scratch,
                     SKV_NOALLOC_SCRATCH_BYTES, d_status, h_total_bytes, stream);
+}
+
+int skv_selftest_lookback(uint64_t* d_state, uint32_t n_chunks, uint32_t missing_chunk, uint32_t max_spins,
+                          uint64_t* d_excl, uint32_t* d_status, void* stream) {
+  if (!d_state || !d_excl || !d_status || n_chunks == 0 || n_chunks > 4096 || max_spins == 0)
+    return SKV_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int st = cuda_status(cudaMemsetAsync(d_state, 0, (size_t)n_chunks * 8, s));
+  if (st == SKV_OK) st = cuda_status(cudaMemsetAsync(d_status, 0, 4, s));
+  if (st == SKV_OK) st = cuda_status(cudaMemsetAsync(d_excl, 0xFF, (size_t)n_chunks * 8, s));
+  if (st != SKV_OK) return st;
+  const uint32_t warps_per_block = 8;
+  k_selftest_lookback<<<(n_chunks + warps_per_block - 1) / warps_per_block, warps_per_block * 32, 0, s>>>(
+      reinterpret_cast<unsigned long long*>(d_state), n_chunks, missing_chunk, max_spins, d_status,
+      reinterpret_cast<unsigned long long*>(d_excl));
+  return launch_check();
 }
 
 int skv_read_status(const uint32_t* d_status, void* stream) {

@@ -314,3 +314,31 @@ def test_empty(nat):
     assert int(codec.lane_offsets[0]) == 0
     codec.decode(t, t)
     assert codec.check() == nat.SKV_OK
+
+
+@pytest.mark.parametrize("n,missing", [(64, 20), (300, 0), (200, 199)])
+def test_lookback_gives_up_without_hanging(nat, n, missing):
+    """the encoder's chunk look-back: predecessors' prefixes are exact, a chunk that
+    never publishes makes its successor time out (bounded polling) and later chunks
+    fail at once; the context stays usable afterwards"""
+    import time
+    state = torch.zeros(n, dtype=torch.int64, device="cuda")
+    excl = torch.zeros(n, dtype=torch.int64, device="cuda")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    t0 = time.perf_counter()
+    assert nat.skv_selftest_lookback(state, n, missing, 2000, excl, status) == nat.SKV_OK
+    st = nat.skv_read_status(status)
+    dt = time.perf_counter() - t0
+    e = excl.cpu().numpy().astype(np.uint64)
+    for w in range(missing):
+        assert int(e[w]) == w * (w + 1) // 2          # sum of totals 1..w
+    for w in range(missing + 1, n):
+        assert int(e[w]) == (1 << 64) - 1
+    assert st == (nat.SKV_ERR_TIMEOUT if missing + 1 < n else nat.SKV_OK)
+    assert dt < 10.0
+    # a normal call still works afterwards
+    ok = torch.zeros(n, dtype=torch.int64, device="cuda")
+    assert nat.skv_selftest_lookback(ok, n, n + 5, 2000, excl, status) == nat.SKV_OK
+    assert nat.skv_read_status(status) == nat.SKV_OK
+    e = excl.cpu().numpy()
+    assert all(int(e[w]) == w * (w + 1) // 2 for w in range(n))
