@@ -342,3 +342,57 @@ def test_lookback_gives_up_without_hanging(nat, n, missing):
     assert nat.skv_read_status(status) == nat.SKV_OK
     e = excl.cpu().numpy()
     assert all(int(e[w]) == w * (w + 1) // 2 for w in range(n))
+
+
+def _adversarial(kind, dtype, n, seed):
+    rng = np.random.default_rng(seed)
+    if dtype == synth.FP8:
+        hi, dt = 256, np.uint8
+        nan, neg0, maxv = 0x7F, 0x80, 0x7E
+    else:
+        hi, dt = 1 << 16, np.uint16
+        nan, neg0, maxv = 0x7FC0, 0x8000, 0x7F7F
+    if kind == "uniform":                    # residuals everywhere: many escapes
+        t, p = rng.integers(0, hi, n), rng.integers(0, hi, n)
+    elif kind == "nan":                      # all NaN target, zero prediction
+        t, p = np.full(n, nan), np.zeros(n, np.int64)
+    elif kind == "signflip":                 # prediction = target with the sign bit flipped
+        t = rng.integers(0, hi, n)
+        p = t ^ (hi >> 1)
+    elif kind == "extremes":                 # largest magnitudes against -0 / +0
+        t = np.where(rng.random(n) < 0.5, maxv, maxv | (hi >> 1))
+        p = np.where(rng.random(n) < 0.5, neg0, 0)
+    else:                                    # mixture: mostly near, 1% wild
+        t = rng.integers(0, hi, n)
+        p = np.where(rng.random(n) < 0.01, rng.integers(0, hi, n), np.clip(t + rng.integers(-2, 3, n), 0, hi - 1))
+    return t.astype(dt), p.astype(dt)
+
+
+@pytest.mark.parametrize("dtype", [synth.FP8, synth.BF16])
+@pytest.mark.parametrize("kind", ["uniform", "nan", "signflip", "extremes", "mixture"])
+def test_adversarial_bit_exact(nat, dtype, kind):
+    """escape-heavy and special-value inputs: GPU stream == oracle stream, exact decode"""
+    L, KV, H, T, D = 2, 2, 2, 700, 128
+    K = 256 if dtype == synth.FP8 else 128
+    n = L * KV * H * T * D
+    tn, pn = _adversarial(kind, dtype, n, seed=hash(kind) % 1000 + dtype)
+    po = oracle.kv_params(dtype, L, KV, H, D, T, K, 256)
+    bins, _, _ = oracle.calibrate(po, tn, pn)
+    fr, cum = oracle.build_tables(po)
+    st, bs, offs = oracle.encode(po, fr, cum, bins, tn, pn)
+    assert st == oracle.OK
+    tdt = torch.uint8 if dtype == synth.FP8 else torch.int16
+    td = torch.from_numpy(tn.view(np.int16) if dtype == synth.BF16 else tn).to(tdt).cuda()
+    pd = torch.from_numpy(pn.view(np.int16) if dtype == synth.BF16 else pn).to(tdt).cuda()
+    codec = nat.Codec(nat.kv_params(dtype, L, KV, H, D, T, K, 256))
+    codec.calibrate(td, pd)
+    codec.build_tables()
+    total = codec.encode(td, pd)
+    assert codec.check() == nat.SKV_OK
+    assert np.array_equal(codec.bins[: bins.size].cpu().numpy(), bins)
+    assert total == bs.size
+    assert np.array_equal(codec.bitstream[:total].cpu().numpy(), bs)
+    assert np.array_equal(codec.lane_offsets.cpu().numpy().astype(np.uint64), offs)
+    out = torch.empty_like(td)
+    codec.decode(pd, out)
+    assert codec.check() == nat.SKV_OK and torch.equal(out, td)
