@@ -53,7 +53,6 @@ constexpr uint32_t kCoefTables = 1024;
 constexpr uint32_t kEncTabStride = 2048 + 40;
 constexpr uint32_t kEncTabBytes = kKvTables * kEncTabStride;       // 66816
 constexpr uint32_t kEmitBytes = 144;                               // per-lane word buffer
-constexpr uint32_t kEmitFlush = 80;                                // flush threshold (bytes)
 constexpr uint32_t kDecTabStride = 4096 + 1024 + 20;
 constexpr uint32_t kDecTabBytes = kKvTables * kDecTabStride;       // 164480
 constexpr uint32_t kRingBytes = 64;                                // per-lane stream ring
@@ -62,7 +61,7 @@ constexpr uint32_t kRingBytes = 64;                                // per-lane s
 #endif
 constexpr int kCodecThreads = SKV_CODEC_THREADS;   // decoder threads per CTA (one CTA per SM)
 #ifndef SKV_ENC_THREADS
-#define SKV_ENC_THREADS 1024
+#define SKV_ENC_THREADS 768
 #endif
 constexpr int kEncThreads = SKV_ENC_THREADS;       // encoder threads per CTA (more registers per thread)
 constexpr int kScanPerBlock = 4096;       // lanes per scan block (256 threads x 16)
@@ -131,14 +130,14 @@ struct WsLayout {
   uint64_t n_scan_blocks, n_slots;
 };
 
-// KV: per-warp lane slots (reused chunk after chunk) + chunk look-back states
+// KV: two sets of lane slots per warp (reused chunk after chunk) + chunk look-back states
 // + the chunk ticket.  COEF: per-lane slots + lane lengths + scan partials.
 WsLayout ws_layout(const Geo& g) {
   WsLayout w;
   memset(&w, 0, sizeof(w));
   if (g.dtype != SKV_COEF_I16) {
     const uint64_t warps = g.n_chunks < kMaxWarps ? g.n_chunks : kMaxWarps;
-    w.n_slots = warps * kLanes;
+    w.n_slots = warps * kLanes * 2;   // two slot sets per warp: one coding, one awaiting placement
     w.slots_off = 0;
     w.state_off = align256(w.n_slots * g.slot_words * 2);
     w.ticket_off = w.state_off + align256(g.n_chunks * 8);
@@ -638,20 +637,33 @@ __device__ __forceinline__ void load_lane_tables(const CodecArgs& a, uint64_t sl
   if (bad) atomicOr(a.status, SKV_FLAG_BAD_BIN);
 }
 
-// Flush the oldest complete 16-byte blocks of a lane's word buffer (the top of
-// the downward-growing buffer) to its global scratch slot, downward from gp;
-// the remaining partial block moves to the top.  With all = true every block
-// goes out, the lowest one padded below the lane's first word.
-__device__ __forceinline__ void emit_flush(uint32_t buf_top, uint32_t& rp, uint8_t*& gp, bool all) {
+// Flush the oldest complete 16-byte blocks of every lane's word buffer (the
+// top of the downward-growing buffer) to the lane's global scratch slot,
+// downward from gp; the remaining partial block moves to the top.  All lanes
+// in act call it together, so the warp pays for one flush loop at a time.
+__device__ __forceinline__ void emit_flush_sync(uint32_t act, uint32_t buf_top, uint32_t& rp, uint8_t*& gp) {
   const uint32_t fill = buf_top - rp;
-  const uint32_t nb = all ? (fill + 15) >> 4 : fill >> 4;
+  const uint32_t nb = fill >> 4, rem = fill & 15u;
+  const uint32_t nmax = __reduce_max_sync(act, nb);
+  for (uint32_t j = 1; j <= nmax; ++j)
+    if (j <= nb) stg_u128(gp - 16 * j, lds_u128(buf_top - 16 * j));
+  gp -= 16 * nb;
+  if (nb != 0 && rem != 0) sts_u128(buf_top - 16, lds_u128(buf_top - 16 * nb - 16));
+  rp = buf_top - rem;
+}
+// Final flush of one lane: every block, the lowest one padded below the
+// lane's first word.
+__device__ __forceinline__ void emit_flush_all(uint32_t buf_top, uint32_t rp, uint8_t*& gp) {
+  const uint32_t nb = (buf_top - rp + 15) >> 4;
   for (uint32_t j = 1; j <= nb; ++j) stg_u128(gp - 16 * j, lds_u128(buf_top - 16 * j));
   gp -= 16 * nb;
-  if (!all) {
-    const uint32_t rem = fill & 15;
-    if (rem) sts_u128(buf_top - 16, lds_u128(buf_top - 16 * nb - 16));
-    rp = buf_top - rem;
-  }
+}
+
+// max of the unsigned 16-bit halves
+__device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 // ---- decoupled look-back over chunks -------------------------------------
@@ -676,15 +688,20 @@ __device__ __forceinline__ unsigned long long warp_sum64(unsigned long long v) {
   return v;
 }
 
-// Exclusive byte prefix of chunk c (whole warp calls); ~0 if it failed.
-__device__ unsigned long long chunk_lookback(unsigned long long* st, uint64_t c, unsigned long long total,
-                                             uint32_t* status, uint32_t max_spins) {
+// Publish chunk c's byte total (whole warp calls): chunk 0 publishes its
+// inclusive prefix at once, every other chunk its aggregate.
+__device__ __forceinline__ void chunk_publish(unsigned long long* st, uint64_t c, unsigned long long total) {
+  if ((threadIdx.x & 31) == 0) st_release(&st[c], (c == 0 ? kStInc : kStAgg) | total);
+}
+
+// Exclusive byte prefix of chunk c, whose aggregate is already published
+// (whole warp calls): walks back over the predecessors 32 at a time, adding
+// aggregates until an inclusive prefix, waiting (bounded) on any that is
+// still coding; then publishes c's inclusive prefix.  ~0 if it failed.
+__device__ unsigned long long chunk_resolve(unsigned long long* st, uint64_t c, unsigned long long total,
+                                            uint32_t* status, uint32_t max_spins) {
   const uint32_t tid = threadIdx.x & 31;
-  if (c == 0) {
-    if (tid == 0) st_release(&st[0], kStInc | total);
-    return 0;
-  }
-  if (tid == 0) st_release(&st[c], kStAgg | total);
+  if (c == 0) return 0;
   unsigned long long excl = 0;
   long long j = (long long)c - 1;
   uint32_t spins = 0;
@@ -704,7 +721,7 @@ __device__ unsigned long long chunk_lookback(unsigned long long* st, uint64_t c,
     if (stop && ((v >> 62) == 3) && tid == (uint32_t)(__ffs(stop) - 1)) failed = true;
     failed = __any_sync(0xFFFFFFFFu, failed);
     if (failed) break;
-    excl += warp_sum64((tid < 32 && (upto >> tid) & 1) ? (v & kStVal) : 0ull);
+    excl += warp_sum64(((upto >> tid) & 1) ? (v & kStVal) : 0ull);
     if (stop) break;
     j -= 32;
   }
@@ -717,6 +734,13 @@ __device__ unsigned long long chunk_lookback(unsigned long long* st, uint64_t c,
   }
   if (tid == 0) st_release(&st[c], kStInc | (excl + total));
   return excl;
+}
+
+// Both steps at once (the self-test's use).
+__device__ unsigned long long chunk_lookback(unsigned long long* st, uint64_t c, unsigned long long total,
+                                             uint32_t* status, uint32_t max_spins) {
+  chunk_publish(st, c, total);
+  return chunk_resolve(st, c, total, status, max_spins);
 }
 
 // Warp-cooperative copy of n_w 16-bit words from src to dst (both 2-byte
@@ -765,9 +789,41 @@ __device__ __forceinline__ void warp_copy_words(uint16_t* dst, const uint16_t* s
   if ((n_w & 1) && tid == 0) dst[n_w - 1] = src[n_w - 1];
 }
 
+// Place a coded chunk whose total is published (whole warp calls): resolve
+// its byte offset, write its lane offsets, copy its 32 lane streams from the
+// slot set `sset` into the bitstream.  len / incl are this thread's format
+// lane length and inclusive prefix within the chunk.
+__device__ __noinline__ void place_chunk(const CodecArgs& a, unsigned long long chunk, unsigned long long total,
+                                         uint32_t len, uint32_t incl, uint64_t sset, uint32_t CS, uint32_t R) {
+  const uint32_t tid = threadIdx.x & 31;
+  const unsigned long long excl = chunk_resolve(a.chunk_state, chunk, total, a.status, kMaxSpins);
+  if (excl == ~0ull) return;
+  const unsigned long long lane_off = excl + incl - len;
+  a.lane_offsets[chunk * kLanes + tid] = lane_off;
+  if (chunk + 1 == a.n_chunks && tid == 31) a.lane_offsets[a.n_lanes] = excl + total;
+  if (excl + total > a.cap) {
+    if (tid == 0) atomicOr(a.status, SKV_FLAG_CAPACITY);
+    return;
+  }
+  __syncwarp();
+  for (uint32_t l = 0; l < kLanes; ++l) {
+    const uint32_t n_w = __shfl_sync(0xFFFFFFFFu, len, l) >> 1;
+    const unsigned long long dst = __shfl_sync(0xFFFFFFFFu, lane_off, l);
+    const uint32_t owner = (l % CS) * R + l / CS;
+    const uint16_t* src = reinterpret_cast<const uint16_t*>(
+        reinterpret_cast<const uint8_t*>(a.slots + (sset * kLanes + owner + 1) * a.slot_words)) - n_w;
+    warp_copy_words(reinterpret_cast<uint16_t*>(a.out_bs + dst), src, n_w, tid);
+  }
+  __syncwarp();
+}
+
 template <int ESZ>
 __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
   constexpr int G = 16 / ESZ;
+  // Room the word buffer must have before a group: a symbol step emits at
+  // most one word, an escaped position adds at most ESZ raw words.
+  constexpr uint32_t kRoomPlain = kEmitBytes - 2 * G;
+  constexpr uint32_t kRoomEsc = kEmitBytes - 2 * G * (1 + ESZ);
   uint8_t* const smem = g_smem;
   // stage the 32 encoder tables (8-byte entries)
   for (uint32_t k = threadIdx.x; k < kKvTables * 256; k += blockDim.x) {
@@ -776,23 +832,31 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
         reinterpret_cast<const uint2*>(a.tables + (uint64_t)t * SKV_TABLE_STRIDE + SKV_TABLE_ENC_OFF)[sidx];
   }
   __syncthreads();
-  const uint32_t tab0 = 0;   // offsets into g_smem
   const uint32_t tid = threadIdx.x & 31;
   // threads take lanes so that the R lanes sharing a channel set are adjacent:
   // a half-warp's table reads then touch at most 16/R channel sets
   const uint32_t R = 32u * G / a.D, CS = 32u / R;
   const uint32_t lane = (tid % R) * CS + tid / R;
   const uint32_t owner_of_tid = (tid % CS) * R + tid / CS;    // thread coding format lane tid
-  const uint32_t buf_top = tab0 + kEncTabBytes + (threadIdx.x + 1) * kEmitBytes;
+  const uint32_t buf_top = kEncTabBytes + (threadIdx.x + 1) * kEmitBytes;
   const uint64_t warp_gid = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (warp_gid >= a.slot_warps) return;   // the workspace holds slots for slot_warps warps only
-  uint8_t* const my_slot_end = reinterpret_cast<uint8_t*>(a.slots + (warp_gid * kLanes + tid + 1) * a.slot_words);
   const uint64_t chunk_pos = (uint64_t)kLanes * a.K;
+  // A coded chunk waits in its slot set until the warp has coded the next
+  // one; by then its predecessors have published their totals, so placing it
+  // rarely waits.
+  unsigned long long pend = ~0ull, pend_total = 0;
+  uint32_t pend_len = 0, pend_incl = 0, set = 0;
   while (true) {
     unsigned long long chunk = 0;
     if (tid == 0) chunk = atomicAdd(a.ticket, 1ull);
     chunk = __shfl_sync(0xFFFFFFFFu, chunk, 0);
-    if (chunk >= a.n_chunks) break;
+    if (chunk >= a.n_chunks) {
+      if (pend != ~0ull) place_chunk(a, pend, pend_total, pend_len, pend_incl, warp_gid * 2 + (set ^ 1u), CS, R);
+      break;
+    }
+    uint8_t* const my_slot_end =
+        reinterpret_cast<uint8_t*>(a.slots + ((warp_gid * 2 + set) * kLanes + tid + 1) * a.slot_words);
     const uint64_t slice = chunk / a.cps;
     const uint64_t first = (chunk - slice * a.cps) * chunk_pos;
     const uint64_t n_pos = min(chunk_pos, a.slice_pos - first);
@@ -801,8 +865,6 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
     const int n_iter = (int)((n_groups + 31) / 32);            // warp-uniform (lane 0 has the most)
     uint32_t tb[G];
     load_lane_tables<ESZ>(a, slice, (lane * G) % a.D, kEncTabStride, tb);
-#pragma unroll
-    for (int e = 0; e < G; ++e) tb[e] += tab0;
     const uint64_t off = (slice * a.slice_pos + first) * ESZ + lane * 16;
     uint8_t* gp = my_slot_end;
     uint32_t rp = buf_top;
@@ -813,9 +875,6 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
       pc = ldg_stream(a.prd + off + (uint64_t)(n_g - 1) * 512);
     }
     for (int i = n_iter - 1; i >= 0; --i) {
-      if (__any_sync(0xFFFFFFFFu, buf_top - rp >= kEmitFlush)) {
-        if (buf_top - rp >= kEmitFlush) emit_flush(buf_top, rp, gp, false);
-      }
       const uint32_t act = __ballot_sync(0xFFFFFFFFu, i < (int)n_g);
       if (i >= (int)n_g) continue;
       uint4 tn = tc, pn = pc;
@@ -823,54 +882,83 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
         tn = ldg_stream(a.tgt + off + (uint64_t)(i - 1) * 512);
         pn = ldg_stream(a.prd + off + (uint64_t)(i - 1) * 512);
       }
-      uint32_t tw[4], pw[4];
+      // FP8: word k of the group gives its even bytes in ve[k] and its odd
+      // bytes in vo[k] as 16-bit lanes ord(t) + 127 - ord(p), which are the
+      // symbols while no position of the group escapes (a negative lane
+      // borrows from the next, which only matters when the group escapes).
+      // The escape test is on the lane-wise maximum: some lane >= 255
+      // exactly when a position needs the escape or a lane went negative.
+      // BF16: the symbols of the two halves of each word, tested directly.
+      uint32_t ve[4], vo[4];
+      bool esc;
+      if (ESZ == 1) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        tw[k] = ESZ == 1 ? ord8x4(word_of(tc, k)) : ord16x2(word_of(tc, k));
-        pw[k] = ESZ == 1 ? ord8x4(word_of(pc, k)) : ord16x2(word_of(pc, k));
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t ot = ord8x4(word_of(tc, k)), op = ord8x4(word_of(pc, k));
+          uint32_t oto, opo;
+          asm("prmt.b32 %0, %1, 0, 0x4341;" : "=r"(oto) : "r"(ot));
+          asm("prmt.b32 %0, %1, 0, 0x4341;" : "=r"(opo) : "r"(op));
+          ve[k] = (ot & 0x00FF00FFu) + 0x007F007Fu - (op & 0x00FF00FFu);
+          vo[k] = oto + 0x007F007Fu - opo;
+        }
+        const uint32_t mx = vmax_u16x2(vmax_u16x2(vmax_u16x2(ve[0], vo[0]), vmax_u16x2(ve[1], vo[1])),
+                                       vmax_u16x2(vmax_u16x2(ve[2], vo[2]), vmax_u16x2(ve[3], vo[3])));
+        esc = ((mx | (mx + 0x00010001u)) & 0xFF00FF00u) != 0u;
+      } else {
+        uint32_t mx = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t ot = ord16x2(word_of(tc, k)), op = ord16x2(word_of(pc, k));
+          ve[k] = (ot & 0xFFFFu) + 127u - (op & 0xFFFFu);
+          vo[k] = (ot >> 16) + 127u - (op >> 16);
+          mx = max(mx, max(ve[k], vo[k]));
+        }
+        esc = mx > 254u;
       }
-      // blocks of 4 positions, highest first: symbols of the block up front and
-      // one warp-uniform test for escapes (rare) per block
+      if (__any_sync(act, esc)) {
+        // rare: exact residuals per position, raw steps where one escapes
+        if (__any_sync(act, buf_top - rp > kRoomEsc)) emit_flush_sync(act, buf_top, rp, gp);
 #pragma unroll
-      for (int blk = G / 4 - 1; blk >= 0; --blk) {
-        constexpr uint32_t mk = ESZ == 1 ? 0xFFu : 0xFFFFu;
-        int rr[4];
-        uint32_t sy[4];
-        bool esc = false;
-#pragma unroll
-        for (int j = 3; j >= 0; --j) {
-          const int e = blk * 4 + j;
+        for (int e = G - 1; e >= 0; --e) {
+          constexpr uint32_t mk = ESZ == 1 ? 0xFFu : 0xFFFFu;
           const uint32_t sh = ESZ == 1 ? 8 * (e & 3) : 16 * (e & 1);
           const int wi = ESZ == 1 ? (e >> 2) : (e >> 1);
-          rr[j] = (int)((tw[wi] >> sh) & mk) - (int)((pw[wi] >> sh) & mk);
-          sy[j] = (uint32_t)(rr[j] + 127);
-          esc |= sy[j] > 254u;
+          const uint32_t ot = ESZ == 1 ? ord8x4(word_of(tc, wi)) : ord16x2(word_of(tc, wi));
+          const uint32_t op = ESZ == 1 ? ord8x4(word_of(pc, wi)) : ord16x2(word_of(pc, wi));
+          const int r = (int)((ot >> sh) & mk) - (int)((op >> sh) & mk);
+          const uint32_t sy = (uint32_t)(r + 127);
+          const bool e_j = sy > 254u;
+          const uint32_t raw = (uint32_t)r & mk;
+          enc_raw_smem_if(x, rp, raw & 0xFFu, e_j);
+          if (ESZ == 2) enc_raw_smem_if(x, rp, raw >> 8, e_j);
+          enc_step_smem(x, rp, lds_u64(tb[e] + (e_j ? 255u : sy) * 8u));
         }
-        if (__any_sync(act, esc)) {
+      } else {
+        if (__any_sync(act, buf_top - rp > kRoomPlain)) emit_flush_sync(act, buf_top, rp, gp);
 #pragma unroll
-          for (int j = 3; j >= 0; --j) {
-            const bool e_j = sy[j] > 254u;
-            const uint32_t raw = (uint32_t)rr[j] & mk;
-            enc_raw_smem_if(x, rp, raw & 0xFFu, e_j);
-            if (ESZ == 2) enc_raw_smem_if(x, rp, raw >> 8, e_j);
-            enc_step_smem(x, rp, lds_u64(tb[blk * 4 + j] + (e_j ? 255u : sy[j]) * 8));
+        for (int e = G - 1; e >= 0; --e) {
+          uint32_t sy;
+          if (ESZ == 1) {
+            const uint32_t v = (e & 1) ? vo[e >> 2] : ve[e >> 2];
+            sy = (e & 2) ? (v >> 16) : (v & 0xFFFFu);
+          } else {
+            sy = (e & 1) ? vo[e >> 1] : ve[e >> 1];
           }
-        } else {
-#pragma unroll
-          for (int j = 3; j >= 0; --j) enc_step_smem(x, rp, lds_u64(tb[blk * 4 + j] + sy[j] * 8));
+          enc_step_smem(x, rp, lds_u64(tb[e] + sy * 8u));
         }
       }
       tc = tn;
       pc = pn;
     }
-    if (buf_top - rp >= kEmitFlush) emit_flush(buf_top, rp, gp, false);
+    // room for the two state words, which go out last (read first)
+    if (__any_sync(0xFFFFFFFFu, buf_top - rp > kEmitBytes - 4)) emit_flush_sync(0xFFFFFFFFu, buf_top, rp, gp);
     rp -= 2;
     sts_u16(rp, x & 0xFFFFu);
     rp -= 2;
     sts_u16(rp, x >> 16);
     const uint32_t my_bytes = (uint32_t)(my_slot_end - gp) + (buf_top - rp);
-    emit_flush(buf_top, rp, gp, true);
-    // lane lengths in format-lane order, chunk total, place the chunk
+    emit_flush_all(buf_top, rp, gp);
+    // lane lengths in format-lane order and the chunk total
     const uint32_t len = __shfl_sync(0xFFFFFFFFu, my_bytes, owner_of_tid);
     uint32_t incl = len;
     for (int o = 1; o < 32; o <<= 1) {
@@ -878,28 +966,13 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
       if (tid >= (uint32_t)o) incl += u;
     }
     const unsigned long long total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-    // pull this thread's own lane stream toward L2 while the look-back polls
-    for (uint32_t o = 0; o < my_bytes; o += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(my_slot_end - my_bytes + o));
-    const unsigned long long excl = chunk_lookback(a.chunk_state, chunk, total, a.status, kMaxSpins);
-    if (excl == ~0ull) continue;
-    const unsigned long long lane_off = excl + incl - len;
-    a.lane_offsets[chunk * kLanes + tid] = lane_off;
-    if (chunk + 1 == a.n_chunks && tid == 31) a.lane_offsets[a.n_lanes] = excl + total;
-    if (excl + total > a.cap) {
-      if (tid == 0) atomicOr(a.status, SKV_FLAG_CAPACITY);
-      continue;
-    }
-    __syncwarp();
-    // copy the 32 lane streams (contiguous in the output) from the slots
-    for (uint32_t l = 0; l < kLanes; ++l) {
-      const uint32_t n_w = __shfl_sync(0xFFFFFFFFu, len, l) >> 1;
-      const unsigned long long dst = __shfl_sync(0xFFFFFFFFu, lane_off, l);
-      const uint32_t owner = (l % CS) * R + l / CS;
-      const uint16_t* src = reinterpret_cast<const uint16_t*>(
-          reinterpret_cast<const uint8_t*>(a.slots + (warp_gid * kLanes + owner + 1) * a.slot_words)) - n_w;
-      warp_copy_words(reinterpret_cast<uint16_t*>(a.out_bs + dst), src, n_w, tid);
-    }
-    __syncwarp();
+    chunk_publish(a.chunk_state, chunk, total);
+    if (pend != ~0ull) place_chunk(a, pend, pend_total, pend_len, pend_incl, warp_gid * 2 + (set ^ 1u), CS, R);
+    pend = chunk;
+    pend_total = total;
+    pend_len = len;
+    pend_incl = incl;
+    set ^= 1u;
   }
 }
 
@@ -1397,7 +1470,7 @@ int skv_encode(const skv_params* p, const void* d_target, const void* d_pred, co
     a.lane_offsets = d_lane_offsets;
     a.out_bs = static_cast<uint8_t*>(d_bitstream);
     a.cap = cap_bytes;
-    a.slot_warps = wl.n_slots / kLanes;
+    a.slot_warps = wl.n_slots / (2 * kLanes);
     st = cuda_status(cudaMemsetAsync(ws + wl.state_off, 0, wl.total - wl.state_off, s));
     if (st != SKV_OK) return st;
     codec_grid(g.n_chunks, &blocks, &threads, kEncThreads);
