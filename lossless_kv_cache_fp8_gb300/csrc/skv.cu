@@ -57,7 +57,7 @@ constexpr uint32_t kDecTabStride = 4096 + 1024 + 20;
 constexpr uint32_t kDecTabBytes = kKvTables * kDecTabStride;       // 164480
 constexpr uint32_t kRingBytes = 64;                                // per-lane stream ring
 #ifndef SKV_CODEC_THREADS
-#define SKV_CODEC_THREADS 1024
+#define SKV_CODEC_THREADS 768
 #endif
 constexpr int kCodecThreads = SKV_CODEC_THREADS;   // decoder threads per CTA (one CTA per SM)
 #ifndef SKV_ENC_THREADS
@@ -384,6 +384,16 @@ __device__ __forceinline__ void ring_open(RingLane& L, const uint8_t* bs, uint32
   L.p += 4;
   L.nxt = ring_word(L, L.p);
   if (L.x < kStateLow && status) atomicOr(status, SKV_FLAG_CORRUPT);
+}
+// Reposition the ring at stream offset p (relative to base, at or after the
+// lane's first byte): reload the four blocks from p's block on and the staged
+// block after them.
+__device__ __forceinline__ void ring_reopen(RingLane& L, uint32_t p) {
+  const uint32_t first = p >> 4;
+  for (uint32_t k = first; k < first + 4; ++k) sts_u128(L.ring + (k & 3u) * 16u, load_block(L, k));
+  L.p = p;
+  L.rb = first + 4;
+  L.stage = load_block(L, L.rb);
 }
 __device__ __forceinline__ void ring_close(const RingLane& L, uint32_t* status) {
   if (L.x != kStateLow || L.p != L.end) atomicOr(status, SKV_FLAG_CORRUPT);
@@ -993,10 +1003,37 @@ __global__ void k_selftest_lookback(unsigned long long* st, uint32_t n, uint32_t
 // up in the shared slot->symbol table, rebuilds the target from the
 // prediction's ordinal and stores whole 16-byte groups.
 // ---------------------------------------------------------------------------
+// Decode one position exactly (escapes included) and add its symbol term to
+// the packed word sw: for a plain symbol the term is sym << sh, for an escape
+// it is (t - p + 127) << sh with t = (p + raw) mod 2^W, so that in every case
+// ord(target word) = ord(prediction word) + sw - 127 per element, exactly.
+template <int ESZ>
+__device__ __forceinline__ void dec_exact(RingLane& L, uint32_t tbe, uint32_t pwd, uint32_t sh, uint32_t act,
+                                          uint32_t& sw) {
+  constexpr uint32_t mk = ESZ == 1 ? 0xFFu : 0xFFFFu;
+  const uint32_t slot = L.x & 4095u;
+  const uint32_t sym = lds_u8(tbe + slot);
+  const uint32_t dv = lds_u32(tbe + 4096u + sym * 4u);
+  L.x = (dv & 0xFFFFu) * (L.x >> 12) + slot - (dv >> 16);
+  ring_renorm(L);
+  uint32_t term = sym;
+  // escapes are rare: a warp-uniform test keeps their steps off the common
+  // path; inside, the raw steps are predicated per lane (no nested branch)
+  if (__any_sync(act, sym == 255u)) {
+    const bool esc = sym == 255u;
+    uint32_t v = ring_raw_if(L, esc);
+    if (ESZ == 2) v = (v << 8) | ring_raw_if(L, esc);
+    const uint32_t pe = (pwd >> sh) & mk;
+    term = esc ? ((pe + v) & mk) - pe + 127u : sym;
+  }
+  sw += term << sh;
+}
+
 template <int ESZ>
 __global__ void __launch_bounds__(kCodecThreads, 1) k_decode_kv(CodecArgs a) {
   constexpr int G = 16 / ESZ;
   constexpr int SUB = ESZ == 1 ? 8 : 4;   // at most 32 / 24 stream bytes between refills
+  constexpr uint32_t kBias = ESZ == 1 ? 0x7F7F7F7Fu : 0x007F007Fu;
   uint8_t* const smem = g_smem;
   for (uint32_t k = threadIdx.x; k < kKvTables * 1280; k += blockDim.x) {
     const uint32_t t = k / 1280, w = k % 1280;
@@ -1004,9 +1041,8 @@ __global__ void __launch_bounds__(kCodecThreads, 1) k_decode_kv(CodecArgs a) {
         reinterpret_cast<const uint32_t*>(a.tables + (uint64_t)t * SKV_TABLE_STRIDE + SKV_TABLE_LUT_OFF)[w];
   }
   __syncthreads();
-  const uint32_t tab0 = 0;   // offsets into g_smem
   const uint32_t lane = threadIdx.x & 31;
-  const uint32_t ring = tab0 + kDecTabBytes + threadIdx.x * kRingBytes;
+  const uint32_t ring = kDecTabBytes + threadIdx.x * kRingBytes;
   const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
   const uint64_t chunk_pos = (uint64_t)kLanes * a.K;
   for (uint64_t chunk = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); chunk < a.n_chunks;
@@ -1018,8 +1054,6 @@ __global__ void __launch_bounds__(kCodecThreads, 1) k_decode_kv(CodecArgs a) {
     const uint32_t n_g = lane < n_groups ? (n_groups - lane + 31) / 32 : 0;
     uint32_t tb[G];
     load_lane_tables<ESZ>(a, slice, (lane * G) % a.D, kDecTabStride, tb);
-#pragma unroll
-    for (int e = 0; e < G; ++e) tb[e] += tab0;
     const uint64_t g = chunk * kLanes + lane;
     uint64_t sa, sb;
     const bool ok = lane_span(a.offs, g, a.n_lanes, a.n_bytes, &sa, &sb);
@@ -1035,37 +1069,55 @@ __global__ void __launch_bounds__(kCodecThreads, 1) k_decode_kv(CodecArgs a) {
       if (i >= n_g) continue;
       uint4 pn = pc;
       if (i + 1 < n_g) pn = ldg_stream(pd + (uint64_t)(i + 1) * 512);
-      uint32_t pw[4], ow[4] = {0, 0, 0, 0};
+      uint32_t pw[4], sw[4] = {0, 0, 0, 0};
 #pragma unroll
       for (int k = 0; k < 4; ++k) pw[k] = ESZ == 1 ? ord8x4(word_of(pc, k)) : ord16x2(word_of(pc, k));
+      if (ESZ == 1) {
+        // FP8: the group's 16 positions are decoded assuming no escape; if
+        // any lane met one, those lanes decode the group again from the saved
+        // state (ring reloaded from the stream) with escapes handled.
+        const uint32_t x0 = L.x, p0 = L.p, n0 = L.nxt;
+        bool esc = false;
 #pragma unroll
-      for (int e = 0; e < G; ++e) {
-        constexpr uint32_t mk = ESZ == 1 ? 0xFFu : 0xFFFFu;
-        const uint32_t sh = ESZ == 1 ? 8 * (e & 3) : 16 * (e & 1);
-        const int wi = ESZ == 1 ? (e >> 2) : (e >> 1);
-        if (e % SUB == 0) ring_refill(L, act);
-        const uint32_t slot = L.x & 4095u;
-        const uint32_t sym = lds_u8(tb[e] + slot);
-        const uint32_t dv = lds_u32(tb[e] + 4096u + sym * 4u);
-        L.x = (dv & 0xFFFFu) * (L.x >> 12) + slot - (dv >> 16);
-        ring_renorm(L);
-        uint32_t r = sym - 127u;
-        // escapes are rare: a warp-uniform test keeps their steps off the common
-        // path; inside, the raw steps are predicated per lane (no nested branch)
-        if (__any_sync(act, sym == 255u)) {
-          const bool esc = sym == 255u;
-          uint32_t v = ring_raw_if(L, esc);
-          if (ESZ == 2) v = (v << 8) | ring_raw_if(L, esc);
-          r = esc ? v : r;
+        for (int e = 0; e < G; ++e) {
+          if (e % SUB == 0) ring_refill(L, act);
+          const uint32_t slot = L.x & 4095u;
+          const uint32_t sym = lds_u8(tb[e] + slot);
+          const uint32_t dv = lds_u32(tb[e] + 4096u + sym * 4u);
+          L.x = (dv & 0xFFFFu) * (L.x >> 12) + slot - (dv >> 16);
+          ring_renorm(L);
+          esc |= sym == 255u;
+          sw[e >> 2] += sym << (8 * (e & 3));
         }
-        const uint32_t ut = (((pw[wi] >> sh) & mk) + r) & mk;
-        ow[wi] |= ut << sh;
+        const uint32_t redo = __ballot_sync(act, esc);
+        if (redo) {
+          if (esc) {
+            ring_reopen(L, p0);
+            L.x = x0;
+            L.nxt = n0;
+            sw[0] = sw[1] = sw[2] = sw[3] = 0;
+#pragma unroll
+            for (int e = 0; e < G; ++e) {
+              if (e % SUB == 0 && e) ring_refill(L, redo);
+              dec_exact<ESZ>(L, tb[e], pw[e >> 2], 8 * (e & 3), redo, sw[e >> 2]);
+            }
+          }
+          __syncwarp(act);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < G; ++e) {
+          if (e % SUB == 0) ring_refill(L, act);
+          dec_exact<ESZ>(L, tb[e], pw[e >> 1], 16 * (e & 1), act, sw[e >> 1]);
+        }
       }
+      // ord(target) = ord(prediction) + sw - 127 per element, exact as a
+      // plain 32-bit sum (every element's result lies in its own field)
       uint4 o;
-      o.x = ESZ == 1 ? unord8x4(ow[0]) : unord16x2(ow[0]);
-      o.y = ESZ == 1 ? unord8x4(ow[1]) : unord16x2(ow[1]);
-      o.z = ESZ == 1 ? unord8x4(ow[2]) : unord16x2(ow[2]);
-      o.w = ESZ == 1 ? unord8x4(ow[3]) : unord16x2(ow[3]);
+      o.x = ESZ == 1 ? unord8x4(pw[0] + sw[0] - kBias) : unord16x2(pw[0] + sw[0] - kBias);
+      o.y = ESZ == 1 ? unord8x4(pw[1] + sw[1] - kBias) : unord16x2(pw[1] + sw[1] - kBias);
+      o.z = ESZ == 1 ? unord8x4(pw[2] + sw[2] - kBias) : unord16x2(pw[2] + sw[2] - kBias);
+      o.w = ESZ == 1 ? unord8x4(pw[3] + sw[3] - kBias) : unord16x2(pw[3] + sw[3] - kBias);
       stg_stream(od + (uint64_t)i * 512, o);
       pc = pn;
     }
