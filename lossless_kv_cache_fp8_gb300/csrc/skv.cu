@@ -56,6 +56,10 @@ constexpr uint32_t kEmitBytes = 144;                               // per-lane w
 constexpr uint32_t kDecTabStride = 4096 + 1024 + 20;
 constexpr uint32_t kDecTabBytes = kKvTables * kDecTabStride;       // 164480
 constexpr uint32_t kRingBytes = 64;                                // per-lane stream ring
+#ifndef SKV_RING_STRIDE
+#define SKV_RING_STRIDE 64
+#endif
+constexpr uint32_t kRingStride = SKV_RING_STRIDE;   // spacing of the lanes' rings (16-byte multiple)
 #ifndef SKV_CODEC_THREADS
 #define SKV_CODEC_THREADS 768
 #endif
@@ -336,7 +340,7 @@ __device__ __forceinline__ void ring_refill(RingLane& L, uint32_t act) {
   }
 }
 __device__ __forceinline__ uint32_t ring_word(const RingLane& L, uint32_t p) {
-  return lds_u16((p & 63u) | L.ring);   // ring is 64-byte aligned
+  return lds_u16((p & (kRingBytes - 1)) + L.ring);
 }
 __device__ __forceinline__ void ring_renorm(RingLane& L) {
   if (L.x < kStateLow) {
@@ -947,14 +951,16 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
         if (__any_sync(act, buf_top - rp > kRoomPlain)) emit_flush_sync(act, buf_top, rp, gp);
 #pragma unroll
         for (int e = G - 1; e >= 0; --e) {
-          uint32_t sy;
+          // byte offset of the entry: 8 * symbol (the upper lane's shift
+          // also drops the lower lane, whose value is below 2^13)
+          uint32_t so;
           if (ESZ == 1) {
             const uint32_t v = (e & 1) ? vo[e >> 2] : ve[e >> 2];
-            sy = (e & 2) ? (v >> 16) : (v & 0xFFFFu);
+            so = (e & 2) ? (v >> 13) : ((v & 0xFFFFu) << 3);
           } else {
-            sy = (e & 1) ? vo[e >> 1] : ve[e >> 1];
+            so = ((e & 1) ? vo[e >> 1] : ve[e >> 1]) << 3;
           }
-          enc_step_smem(x, rp, lds_u64(tb[e] + sy * 8u));
+          enc_step_smem(x, rp, lds_u64(tb[e] + so));
         }
       }
       tc = tn;
@@ -1042,7 +1048,7 @@ __global__ void __launch_bounds__(kCodecThreads, 1) k_decode_kv(CodecArgs a) {
   }
   __syncthreads();
   const uint32_t lane = threadIdx.x & 31;
-  const uint32_t ring = kDecTabBytes + threadIdx.x * kRingBytes;
+  const uint32_t ring = kDecTabBytes + threadIdx.x * kRingStride;
   const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
   const uint64_t chunk_pos = (uint64_t)kLanes * a.K;
   for (uint64_t chunk = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); chunk < a.n_chunks;
@@ -1617,12 +1623,12 @@ int skv_decode(const skv_params* p, const void* d_bitstream, uint64_t n_bytes, c
   }
   int blocks, threads;
   codec_grid(g.n_chunks, &blocks, &threads, kCodecThreads);
-  const int smem_bytes = (int)(kDecTabBytes + (uint32_t)threads * kRingBytes);
+  const int smem_bytes = (int)(kDecTabBytes + (uint32_t)threads * kRingStride);
   if (g.esz == 1) {
-    if ((st = set_smem(k_decode_kv<1>, kDecTabBytes + kCodecThreads * kRingBytes)) != SKV_OK) return st;
+    if ((st = set_smem(k_decode_kv<1>, kDecTabBytes + kCodecThreads * kRingStride)) != SKV_OK) return st;
     k_decode_kv<1><<<blocks, threads, smem_bytes, s>>>(a);
   } else {
-    if ((st = set_smem(k_decode_kv<2>, kDecTabBytes + kCodecThreads * kRingBytes)) != SKV_OK) return st;
+    if ((st = set_smem(k_decode_kv<2>, kDecTabBytes + kCodecThreads * kRingStride)) != SKV_OK) return st;
     k_decode_kv<2><<<blocks, threads, smem_bytes, s>>>(a);
   }
   return launch_check();
