@@ -348,9 +348,14 @@ def main_ours(args):
 
 
 def e2e(args, w, codec, tgt, prd, cal, out, stream, dev, total):
-    """same step through the C ABI, inputs from pinned host memory, bitstream read back"""
+    """The same step through the C ABI with the inputs in pinned host memory and the
+    stream read back.  KV caches go through pipeline.HostPipeline (layer groups:
+    host->device copies, coding and the device->host copy of the stream overlap on
+    three streams; the joined stream is checked byte for byte against the one-call
+    stream); coefficient streams are copied in, coded and copied back in sequence."""
+    import numpy as np
     import torch
-    from lossless_kv_cache_fp8_gb300 import synth
+    from lossless_kv_cache_fp8_gb300 import native, pipeline, synth
     try:
         h_t = torch.empty(tgt.shape, dtype=tgt.dtype, pin_memory=True)
         h_p = torch.empty(prd.shape, dtype=prd.dtype, pin_memory=True)
@@ -361,31 +366,48 @@ def e2e(args, w, codec, tgt, prd, cal, out, stream, dev, total):
     h_p.copy_(prd)
     h_off = torch.empty(codec.lane_offsets.shape, dtype=torch.int64, pin_memory=True)
     torch.cuda.synchronize()
+    kv = w.dtype != synth.COEF
+    pipe = None
+    if kv:
+        groups = max(1, min(16, w.n_layers))
+        pipe = pipeline.HostPipeline(codec.p, group_layers=-(-w.n_layers // groups), device=dev,
+                                     cap_frac=args.cap_frac)
+    out.zero_()   # every step must write the whole decoded cache again
     times = []
     nb = 0
     for k in range(args.warmup + max(1, args.e2e_steps)):
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
-        tgt.copy_(h_t, non_blocking=True)
-        prd.copy_(h_p, non_blocking=True)
-        codec.calibrate(None if w.dtype == synth.COEF else tgt, cal)
-        codec.build_tables()
-        n = codec.encode(tgt, prd, want_total=True)
-        h_bs[:n].copy_(codec.bitstream[:n], non_blocking=True)
-        h_off.copy_(codec.lane_offsets, non_blocking=True)
-        codec.decode(prd, out, n_bytes=n)
+        if kv:
+            n = pipe.run(h_t, h_p, h_bs, h_off, decode_into=out, stream=stream)
+        else:
+            tgt.copy_(h_t, non_blocking=True)
+            prd.copy_(h_p, non_blocking=True)
+            codec.calibrate(None, cal)
+            codec.build_tables()
+            n = codec.encode(tgt, prd, want_total=True)
+            h_bs[:n].copy_(codec.bitstream[:n], non_blocking=True)
+            h_off.copy_(codec.lane_offsets, non_blocking=True)
+            codec.decode(prd, out, n_bytes=n)
         t1.record(stream)
         torch.cuda.synchronize()
         if k >= args.warmup:
             times.append(t0.elapsed_time(t1))
         nb = n
     assert torch.equal(out, tgt)
+    res = {}
+    if kv:
+        assert pipe.check() == native.SKV_OK
+        assert nb == total and torch.equal(h_bs[:nb], codec.bitstream[:nb].cpu())
+        assert np.array_equal(pipe.joined_offsets(h_off.numpy()), codec.lane_offsets.cpu().numpy().view(np.uint64))
+        res["pipeline"] = {"layer_groups": len(pipe.groups), "streams": 3,
+                           "check": "joined stream and offsets equal the one-call stream"}
     ms = statistics.mean(times)
     h2d = h_t.numel() * h_t.element_size() + h_p.numel() * h_p.element_size()
     d2h = nb + h_off.numel() * 8
     return {"value": w.raw_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": len(times)}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": len(times), **res}
 
 
 def main():
