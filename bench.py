@@ -339,6 +339,8 @@ def main_ours(args):
         "gpu_launches": (4 if w.dtype != synth.COEF else 8) * args.steps,
         "clocks": clk.summary(),
     }
+    if args.paged and w.dtype != synth.COEF:
+        res["paged"] = paged_run(args, w, codec, tgt, prd, stream, total, peak)
     if args.e2e and world >= 1:
         res["e2e"] = e2e(args, w, codec, tgt, prd, cal, out, stream, dev, total)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -410,6 +412,50 @@ def e2e(args, w, codec, tgt, prd, cal, out, stream, dev, total):
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": len(times), **res}
 
 
+def paged_run(args, w, codec, tgt, prd, stream, total, peak):
+    """encode / decode the same cache held in paged pools (random block table,
+    args.paged tokens per block); the stream must equal the dense one"""
+    import torch
+    from lossless_kv_cache_fp8_gb300 import native, synth
+    B = args.paged
+    tp, pp, table, n_blocks = synth.to_paged(tgt, prd, B, seed=1)
+    lay = native.paged_layout(table, n_blocks, B)
+    p = codec.p
+    bs = torch.empty_like(codec.bitstream)
+    off = torch.empty_like(codec.lane_offsets)
+    outp = torch.zeros_like(tp)
+    status = torch.zeros(4, dtype=torch.int32, device=tgt.device)
+
+    def enc():
+        st, _ = native.skv_encode_paged(p, lay, tp, pp, codec.tables, codec.bins, bs, codec.cap, off,
+                                        codec.workspace, codec.workspace.numel(), status, want_total=False)
+        assert st == native.SKV_OK
+
+    def dec():
+        assert native.skv_decode_paged(p, lay, bs, total, off, pp, codec.tables, codec.bins, outp,
+                                       status) == native.SKV_OK
+
+    ms = {}
+    for name, fn in (("encode", enc), ("decode", dec)):
+        for _ in range(args.warmup):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms[name] = e0.elapsed_time(e1) / args.steps
+        assert native.skv_read_status(status) == native.SKV_OK
+    assert torch.equal(bs[:total], codec.bitstream[:total]) and torch.equal(off, codec.lane_offsets)
+    assert torch.equal(outp, tp)
+    raw = w.raw_bytes
+    moved = 2 * raw + total + 8 * off.numel()
+    return {"block_tokens": B, "n_blocks": n_blocks, "encode_ms": ms["encode"], "decode_ms": ms["decode"],
+            "encode_hbm_frac": moved / ms["encode"] / 1e6 / peak, "decode_hbm_frac": moved / ms["decode"] / 1e6 / peak,
+            "check": "stream, offsets and decoded pool equal the dense call"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -420,6 +466,7 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling cases)")
     ap.add_argument("--cap-frac", type=float, default=0.6, help="bitstream buffer / raw bytes")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--paged", type=int, default=0, help="also time paged pools with this many tokens per block")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -103,6 +103,7 @@ extern "C" {
 #define SKV_FLAG_CAPACITY 2u
 #define SKV_FLAG_TIMEOUT 4u
 #define SKV_FLAG_BAD_BIN 8u
+#define SKV_FLAG_BAD_BLOCK 16u
 
 typedef struct {
   uint32_t version;   /* SKV_PARAMS_VERSION                                     */
@@ -181,6 +182,51 @@ int skv_decode(const skv_params* p, const void* d_bitstream, uint64_t n_bytes,
                const uint64_t* d_lane_offsets, const void* d_pred, const void* d_tables,
                const uint8_t* d_bins, void* d_target_out, uint32_t* d_status, void* stream);
 
+/* Paged KV caches (block pools, as serving systems keep them; [SKV] core idea
+ * for prefill-to-decode transfer and prefix caches).  The pages define no
+ * layout; this one keeps each token's heads and channels together:
+ *   pool (l, kv) of every layer l and K/V index kv holds n_blocks blocks;
+ *   block b holds block_tokens consecutive tokens as [block_tokens][n_heads]
+ *   [head_dim] (row-major); the pools are contiguous, pool (l, kv) first,
+ *   so element (l, kv, b, row, h, d) sits at index
+ *   ((((l * n_kv + kv) * n_blocks + b) * block_tokens + row) * n_heads + h)
+ *   * head_dim + d of d_*_pool (elements of 1 byte for FP8, 2 for BF16).
+ * d_block_table[j] (u32, j < ceil(n_tokens / block_tokens)) is the block that
+ * holds tokens [j * block_tokens, (j + 1) * block_tokens) in every pool; rows
+ * past n_tokens in the last block are not read or written.  block_tokens must
+ * be a power of two.  The caller owns the pools and the table.
+ *
+ * The paged calls compute exactly what the dense calls compute on the cache
+ * gathered into [layer][kv][head][token][head_dim]: the same bins, the same
+ * bitstream and lane offsets, and a decode that writes the target bits into
+ * the target pool's rows (other rows untouched).  KV dtypes only (COEF streams:
+ * SKV_ERR_UNSUPPORTED).  A block-table entry >= n_blocks sets
+ * SKV_FLAG_BAD_BLOCK in d_status (skv_read_status: SKV_ERR_INVALID_ARG); its
+ * rows are then read from block 0 and never written. */
+typedef struct {
+  const uint32_t* d_block_table;
+  uint32_t n_blocks;     /* blocks per (layer, K/V) pool */
+  uint32_t block_tokens; /* tokens per block, a power of two */
+} skv_paged_layout;
+
+/* skv_calibrate on paged pools; d_status (one u32, cleared first) collects
+ * SKV_FLAG_BAD_BLOCK. */
+int skv_calibrate_paged(const skv_params* p, const skv_paged_layout* layout, const void* d_target_pool,
+                        const void* d_pred_pool, uint8_t* d_bins, uint32_t* d_sum_abs, uint32_t* d_hist,
+                        uint32_t* d_status, void* stream);
+
+/* skv_encode on paged pools (same workspace, outputs and status rules). */
+int skv_encode_paged(const skv_params* p, const skv_paged_layout* layout, const void* d_target_pool,
+                     const void* d_pred_pool, const void* d_tables, const uint8_t* d_bins, void* d_bitstream,
+                     uint64_t cap_bytes, uint64_t* d_lane_offsets, void* d_workspace, uint64_t workspace_bytes,
+                     uint32_t* d_status, uint64_t* h_total_bytes, void* stream);
+
+/* skv_decode into the rows of a paged target pool. */
+int skv_decode_paged(const skv_params* p, const skv_paged_layout* layout, const void* d_bitstream,
+                     uint64_t n_bytes, const uint64_t* d_lane_offsets, const void* d_pred_pool,
+                     const void* d_tables, const uint8_t* d_bins, void* d_target_pool_out, uint32_t* d_status,
+                     void* stream);
+
 /* Encode without a caller-provided workspace.  The pages have no counterpart
  * to this call; it exists for callers that cannot allocate device memory, such
  * as code handed only its input and output buffers by a host framework that
@@ -220,7 +266,7 @@ int skv_selftest_lookback(uint64_t* d_state, uint32_t n_chunks, uint32_t missing
 
 /* Synchronises the stream, reads the status word and returns SKV_OK or the
  * code of the most serious flag (CORRUPT > CAPACITY > TIMEOUT > INVALID_ARG
- * for an out-of-range bin). */
+ * for an out-of-range bin or block-table entry). */
 int skv_read_status(const uint32_t* d_status, void* stream);
 
 #ifdef __cplusplus

@@ -403,6 +403,44 @@ __device__ __forceinline__ void ring_close(const RingLane& L, uint32_t* status) 
   if (L.x != kStateLow || L.p != L.end) atomicOr(status, SKV_FLAG_CORRUPT);
 }
 
+// Paged KV pools: pool (layer, k/v) holds n_blocks blocks of 2^shift tokens,
+// each block [tokens][H][D]; bt[j] is the block of tokens [j 2^shift, (j+1) 2^shift).
+// bt == nullptr means the dense [layer][k/v][head][token][D] layout.
+struct Paged {
+  const uint32_t* bt;
+  uint32_t n_blocks, shift, H;
+};
+// Element index, in the paged pools, of token t, channel d of slice
+// (layer, k/v, head); an out-of-range block-table entry flags SKV_FLAG_BAD_BLOCK
+// and yields ok = false (the index then points into block 0).
+__device__ __forceinline__ uint64_t paged_elem(const Paged& pg, uint64_t slice, uint64_t t, uint32_t d, uint32_t D,
+                                               uint32_t* status, bool& ok) {
+  const uint64_t lk = slice / pg.H, h = slice - lk * pg.H;
+  uint32_t blk = __ldg(pg.bt + (t >> pg.shift));
+  ok = blk < pg.n_blocks;
+  if (!ok) {
+    atomicOr(status, SKV_FLAG_BAD_BLOCK);
+    blk = 0;
+  }
+  const uint64_t phys = ((uint64_t)blk << pg.shift) | (t & ((1ull << pg.shift) - 1));
+  return (((lk * pg.n_blocks) << pg.shift) + phys) * ((uint64_t)pg.H * D) + h * D + d;
+}
+
+// The same from a block-table entry read earlier (the codec kernels read the
+// entries of a lane's groups ahead of the group loads): lkb = (layer, k/v)
+// pool's first row, hd0 = h * D + d0.
+__device__ __forceinline__ uint64_t paged_elem_at(const Paged& pg, uint32_t blk, uint64_t t, uint64_t lkb,
+                                                  uint64_t hd0, uint32_t D, uint32_t* status, bool& ok) {
+  ok = blk < pg.n_blocks;
+  if (!ok) {
+    atomicOr(status, SKV_FLAG_BAD_BLOCK);
+    blk = 0;
+  }
+  const uint64_t phys = ((uint64_t)blk << pg.shift) | (t & ((1ull << pg.shift) - 1));
+  return (lkb + phys) * ((uint64_t)pg.H * D) + hd0;
+}
+__device__ __forceinline__ uint32_t paged_entry(const Paged& pg, uint64_t t) { return __ldg(pg.bt + (t >> pg.shift)); }
+
 // lane offsets [a, b) of lane g, checked against the stream
 __device__ __forceinline__ bool lane_span(const uint64_t* offs, uint64_t g, uint64_t n_lanes,
                                           uint64_t n_bytes, uint64_t* a, uint64_t* b) {
@@ -528,11 +566,11 @@ __global__ void __launch_bounds__(256) k_build_tables(uint8_t* blob, uint32_t su
 // channels for a stride of tokens; partial sums are combined across the lanes
 // that share a channel group with warp shuffles, then across warps.
 // ---------------------------------------------------------------------------
-template <int ESZ>
+template <int ESZ, bool PAGED>
 __global__ void __launch_bounds__(256) k_calibrate_kv(const uint8_t* tgt, const uint8_t* prd,
                                                       uint8_t* bins, uint32_t* sum_abs,
                                                       uint32_t* hist, uint64_t T, uint32_t D,
-                                                      uint32_t nc) {
+                                                      uint32_t nc, Paged pg, uint32_t* status) {
   constexpr int G = 16 / ESZ;
   __shared__ unsigned long long S[512];
   const uint64_t slice = blockIdx.x;
@@ -547,7 +585,8 @@ __global__ void __launch_bounds__(256) k_calibrate_kv(const uint8_t* tgt, const 
   const uint64_t base = slice * T * D;          // element index of the slice
   if (tph < nph) {
     for (uint64_t t = tph; t < nc; t += nph) {
-      const uint64_t el = base + t * D + (uint64_t)cg * G;
+      bool ok = true;
+      const uint64_t el = PAGED ? paged_elem(pg, slice, t, cg * G, D, status, ok) : base + t * D + (uint64_t)cg * G;
       const uint4 tv = ldg_stream(tgt + el * ESZ), pv = ldg_stream(prd + el * ESZ);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -626,6 +665,7 @@ struct CodecArgs {
   uint8_t* out_bs;                  // final bitstream
   uint64_t cap;
   uint64_t slot_warps;              // warps that own a slot set in the workspace
+  Paged pg;                         // paged pools (pg.bt == nullptr: dense caches)
 };
 
 template <int ESZ>
@@ -831,7 +871,7 @@ __device__ __noinline__ void place_chunk(const CodecArgs& a, unsigned long long 
   __syncwarp();
 }
 
-template <int ESZ>
+template <int ESZ, bool PAGED>
 __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
   constexpr int G = 16 / ESZ;
   // Room the word buffer must have before a group: a symbol step emits at
@@ -880,21 +920,47 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
     uint32_t tb[G];
     load_lane_tables<ESZ>(a, slice, (lane * G) % a.D, kEncTabStride, tb);
     const uint64_t off = (slice * a.slice_pos + first) * ESZ + lane * 16;
+    // byte offset of this lane's group k of the chunk in the caches
+    const uint32_t tpi = 32u * G / a.D;   // tokens between a lane's consecutive groups
+    const uint64_t tok0 = first / a.D + (lane * G) / a.D;
+    const uint32_t d0 = (lane * G) % a.D;
+    // paged pools: the block-table entries of groups i - 1 and i - 2 are read
+    // while group i is coded (bt1, bt2), so a group load never waits on one
+    const uint64_t lk = PAGED ? slice / a.pg.H : 0;
+    const uint64_t lkb = PAGED ? (lk * a.pg.n_blocks) << a.pg.shift : 0;
+    const uint64_t hd0 = PAGED ? (slice - lk * a.pg.H) * a.D + d0 : 0;
+    auto goff = [&](uint32_t k, uint32_t blk) -> uint64_t {
+      if (!PAGED) return off + (uint64_t)k * 512;
+      bool ok;
+      return paged_elem_at(a.pg, blk, tok0 + (uint64_t)k * tpi, lkb, hd0, a.D, a.status, ok) * ESZ;
+    };
+    auto entry = [&](int k) -> uint32_t {
+      return (PAGED && k >= 0) ? paged_entry(a.pg, tok0 + (uint64_t)k * tpi) : 0u;
+    };
     uint8_t* gp = my_slot_end;
     uint32_t rp = buf_top;
     uint32_t x = kStateLow;
     uint4 tc = make_uint4(0, 0, 0, 0), pc = tc;
+    uint32_t bt1 = 0, bt2 = 0;
     if (n_g) {
-      tc = ldg_stream(a.tgt + off + (uint64_t)(n_g - 1) * 512);
-      pc = ldg_stream(a.prd + off + (uint64_t)(n_g - 1) * 512);
+      const uint64_t o = goff(n_g - 1, entry((int)n_g - 1));
+      tc = ldg_stream(a.tgt + o);
+      pc = ldg_stream(a.prd + o);
+      bt1 = entry((int)n_g - 2);
+      bt2 = entry((int)n_g - 3);
     }
     for (int i = n_iter - 1; i >= 0; --i) {
       const uint32_t act = __ballot_sync(0xFFFFFFFFu, i < (int)n_g);
       if (i >= (int)n_g) continue;
       uint4 tn = tc, pn = pc;
       if (i > 0) {
-        tn = ldg_stream(a.tgt + off + (uint64_t)(i - 1) * 512);
-        pn = ldg_stream(a.prd + off + (uint64_t)(i - 1) * 512);
+        const uint64_t o = goff(i - 1, bt1);
+        tn = ldg_stream(a.tgt + o);
+        pn = ldg_stream(a.prd + o);
+      }
+      if (PAGED) {
+        bt1 = bt2;
+        bt2 = entry(i - 3);
       }
       // FP8: word k of the group gives its even bytes in ve[k] and its odd
       // bytes in vo[k] as 16-bit lanes ord(t) + 127 - ord(p), which are the
@@ -1035,7 +1101,7 @@ __device__ __forceinline__ void dec_exact(RingLane& L, uint32_t tbe, uint32_t pw
   sw += term << sh;
 }
 
-template <int ESZ>
+template <int ESZ, bool PAGED>
 __global__ void __launch_bounds__(kCodecThreads, 1) k_decode_kv(CodecArgs a) {
   constexpr int G = 16 / ESZ;
   constexpr int SUB = ESZ == 1 ? 8 : 4;   // at most 32 / 24 stream bytes between refills
@@ -1065,16 +1131,39 @@ __global__ void __launch_bounds__(kCodecThreads, 1) k_decode_kv(CodecArgs a) {
     const bool ok = lane_span(a.offs, g, a.n_lanes, a.n_bytes, &sa, &sb);
     RingLane L;
     ring_open(L, a.bs, ring, sa, sb, ok, a.status);
-    const uint8_t* pd = a.prd + (slice * a.slice_pos + first) * ESZ + lane * 16;
-    uint8_t* od = a.out + (slice * a.slice_pos + first) * ESZ + lane * 16;
+    const uint64_t off = (slice * a.slice_pos + first) * ESZ + lane * 16;
+    // byte offset of this lane's group k of the chunk in the caches (ok: the
+    // paged block-table entry is in range)
+    const uint32_t tpi = 32u * G / a.D;
+    const uint64_t tok0 = first / a.D + (lane * G) / a.D;
+    const uint32_t d0 = (lane * G) % a.D;
+    // paged pools: entries of groups i + 1 and i + 2 are read ahead (btn1, btn2)
+    const uint64_t lk = PAGED ? slice / a.pg.H : 0;
+    const uint64_t lkb = PAGED ? (lk * a.pg.n_blocks) << a.pg.shift : 0;
+    const uint64_t hd0 = PAGED ? (slice - lk * a.pg.H) * a.D + d0 : 0;
+    auto goff = [&](uint32_t k, uint32_t blk, bool& ok) -> uint64_t {
+      ok = true;
+      if (!PAGED) return off + (uint64_t)k * 512;
+      return paged_elem_at(a.pg, blk, tok0 + (uint64_t)k * tpi, lkb, hd0, a.D, a.status, ok) * ESZ;
+    };
+    auto entry = [&](uint32_t k) -> uint32_t {
+      return (PAGED && k < n_g) ? paged_entry(a.pg, tok0 + (uint64_t)k * tpi) : 0u;
+    };
     uint4 pc = make_uint4(0, 0, 0, 0);
-    if (n_g) pc = ldg_stream(pd);
+    uint32_t btc = entry(0), btn1 = entry(1), btn2 = entry(2);
+    if (n_g) {
+      bool ok;
+      pc = ldg_stream(a.prd + goff(0, btc, ok));
+    }
     const uint32_t n_iter = (n_groups + 31) / 32;              // warp-uniform
     for (uint32_t i = 0; i < n_iter; ++i) {
       const uint32_t act = __ballot_sync(0xFFFFFFFFu, i < n_g);
       if (i >= n_g) continue;
       uint4 pn = pc;
-      if (i + 1 < n_g) pn = ldg_stream(pd + (uint64_t)(i + 1) * 512);
+      if (i + 1 < n_g) {
+        bool ok;
+        pn = ldg_stream(a.prd + goff(i + 1, btn1, ok));
+      }
       uint32_t pw[4], sw[4] = {0, 0, 0, 0};
 #pragma unroll
       for (int k = 0; k < 4; ++k) pw[k] = ESZ == 1 ? ord8x4(word_of(pc, k)) : ord16x2(word_of(pc, k));
@@ -1124,8 +1213,15 @@ __global__ void __launch_bounds__(kCodecThreads, 1) k_decode_kv(CodecArgs a) {
       o.y = ESZ == 1 ? unord8x4(pw[1] + sw[1] - kBias) : unord16x2(pw[1] + sw[1] - kBias);
       o.z = ESZ == 1 ? unord8x4(pw[2] + sw[2] - kBias) : unord16x2(pw[2] + sw[2] - kBias);
       o.w = ESZ == 1 ? unord8x4(pw[3] + sw[3] - kBias) : unord16x2(pw[3] + sw[3] - kBias);
-      stg_stream(od + (uint64_t)i * 512, o);
+      bool ok;
+      const uint64_t oo = goff(i, btc, ok);
+      if (ok) stg_stream(a.out + oo, o);
       pc = pn;
+      if (PAGED) {
+        btc = btn1;
+        btn1 = btn2;
+        btn2 = entry(i + 3);
+      }
     }
     ring_close(L, a.status);
   }
@@ -1437,12 +1533,13 @@ uint64_t skv_encode_workspace_bytes(const skv_params* p) {
   return ws_layout(g).total;
 }
 
-int skv_calibrate(const skv_params* p, const void* d_target, const void* d_pred, uint8_t* d_bins,
-                  uint32_t* d_sum_abs, uint32_t* d_hist, void* stream) {
+static int calibrate_impl(const skv_params* p, const Paged* pg, uint32_t* d_status, const void* d_target,
+                          const void* d_pred, uint8_t* d_bins, uint32_t* d_sum_abs, uint32_t* d_hist, void* stream) {
   Geo g;
   int st = make_geo(p, &g);
   if (st != SKV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (pg && (st = cuda_status(cudaMemsetAsync(d_status, 0, 4, s))) != SKV_OK) return st;
   if (g.n_channels == 0) return SKV_OK;
   if (!d_pred || !d_bins) return SKV_ERR_INVALID_ARG;
   if (g.dtype == SKV_COEF_I16) {
@@ -1453,15 +1550,23 @@ int skv_calibrate(const skv_params* p, const void* d_target, const void* d_pred,
   if (!d_target || !aligned16(d_target) || !aligned16(d_pred)) return SKV_ERR_INVALID_ARG;
   const uint32_t nc = (uint32_t)(p->n_calib < g.T ? p->n_calib : g.T);
   if (g.n_slices > 0x7FFFFFFFull) return SKV_ERR_UNSUPPORTED;
-  if (g.esz == 1)
-    k_calibrate_kv<1><<<(unsigned)g.n_slices, 256, 0, s>>>(static_cast<const uint8_t*>(d_target),
-                                                            static_cast<const uint8_t*>(d_pred), d_bins,
-                                                            d_sum_abs, d_hist, g.T, g.D, nc);
-  else
-    k_calibrate_kv<2><<<(unsigned)g.n_slices, 256, 0, s>>>(static_cast<const uint8_t*>(d_target),
-                                                            static_cast<const uint8_t*>(d_pred), d_bins,
-                                                            d_sum_abs, d_hist, g.T, g.D, nc);
+  const uint8_t* t8 = static_cast<const uint8_t*>(d_target);
+  const uint8_t* p8 = static_cast<const uint8_t*>(d_pred);
+  const Paged dense = {nullptr, 0, 0, 1};
+  const unsigned nb = (unsigned)g.n_slices;
+  if (g.esz == 1) {
+    if (pg) k_calibrate_kv<1, true><<<nb, 256, 0, s>>>(t8, p8, d_bins, d_sum_abs, d_hist, g.T, g.D, nc, *pg, d_status);
+    else k_calibrate_kv<1, false><<<nb, 256, 0, s>>>(t8, p8, d_bins, d_sum_abs, d_hist, g.T, g.D, nc, dense, nullptr);
+  } else {
+    if (pg) k_calibrate_kv<2, true><<<nb, 256, 0, s>>>(t8, p8, d_bins, d_sum_abs, d_hist, g.T, g.D, nc, *pg, d_status);
+    else k_calibrate_kv<2, false><<<nb, 256, 0, s>>>(t8, p8, d_bins, d_sum_abs, d_hist, g.T, g.D, nc, dense, nullptr);
+  }
   return launch_check();
+}
+
+int skv_calibrate(const skv_params* p, const void* d_target, const void* d_pred, uint8_t* d_bins,
+                  uint32_t* d_sum_abs, uint32_t* d_hist, void* stream) {
+  return calibrate_impl(p, nullptr, nullptr, d_target, d_pred, d_bins, d_sum_abs, d_hist, stream);
 }
 
 int skv_build_tables(const skv_params* p, void* d_tables, uint64_t tables_bytes, void* stream) {
@@ -1475,10 +1580,10 @@ int skv_build_tables(const skv_params* p, void* d_tables, uint64_t tables_bytes,
   return launch_check();
 }
 
-int skv_encode(const skv_params* p, const void* d_target, const void* d_pred, const void* d_tables,
-               const uint8_t* d_bins, void* d_bitstream, uint64_t cap_bytes, uint64_t* d_lane_offsets,
-               void* d_workspace, uint64_t workspace_bytes, uint32_t* d_status, uint64_t* h_total_bytes,
-               void* stream) {
+static int encode_impl(const skv_params* p, const Paged* pg, const void* d_target, const void* d_pred,
+                       const void* d_tables, const uint8_t* d_bins, void* d_bitstream, uint64_t cap_bytes,
+                       uint64_t* d_lane_offsets, void* d_workspace, uint64_t workspace_bytes, uint32_t* d_status,
+                       uint64_t* h_total_bytes, void* stream) {
   Geo g;
   int st = make_geo(p, &g);
   if (st != SKV_OK) return st;
@@ -1533,12 +1638,20 @@ int skv_encode(const skv_params* p, const void* d_target, const void* d_pred, co
     if (st != SKV_OK) return st;
     codec_grid(g.n_chunks, &blocks, &threads, kEncThreads);
     const int smem_bytes = (int)(kEncTabBytes + (uint32_t)threads * kEmitBytes);
-    if (g.esz == 1) {
-      if ((st = set_smem(k_encode_kv<1>, kEncTabBytes + kEncThreads * kEmitBytes)) != SKV_OK) return st;
-      k_encode_kv<1><<<blocks, threads, smem_bytes, s>>>(a);
+    const uint32_t smax = kEncTabBytes + kEncThreads * kEmitBytes;
+    if (pg) a.pg = *pg;
+    if (g.esz == 1 && !pg) {
+      if ((st = set_smem(k_encode_kv<1, false>, smax)) != SKV_OK) return st;
+      k_encode_kv<1, false><<<blocks, threads, smem_bytes, s>>>(a);
+    } else if (g.esz == 1) {
+      if ((st = set_smem(k_encode_kv<1, true>, smax)) != SKV_OK) return st;
+      k_encode_kv<1, true><<<blocks, threads, smem_bytes, s>>>(a);
+    } else if (!pg) {
+      if ((st = set_smem(k_encode_kv<2, false>, smax)) != SKV_OK) return st;
+      k_encode_kv<2, false><<<blocks, threads, smem_bytes, s>>>(a);
     } else {
-      if ((st = set_smem(k_encode_kv<2>, kEncTabBytes + kEncThreads * kEmitBytes)) != SKV_OK) return st;
-      k_encode_kv<2><<<blocks, threads, smem_bytes, s>>>(a);
+      if ((st = set_smem(k_encode_kv<2, true>, smax)) != SKV_OK) return st;
+      k_encode_kv<2, true><<<blocks, threads, smem_bytes, s>>>(a);
     }
     if ((st = launch_check()) != SKV_OK) return st;
     if (h_total_bytes) {
@@ -1582,9 +1695,9 @@ int skv_encode(const skv_params* p, const void* d_target, const void* d_pred, co
   return launch_check();
 }
 
-int skv_decode(const skv_params* p, const void* d_bitstream, uint64_t n_bytes, const uint64_t* d_lane_offsets,
-               const void* d_pred, const void* d_tables, const uint8_t* d_bins, void* d_target_out,
-               uint32_t* d_status, void* stream) {
+static int decode_impl(const skv_params* p, const Paged* pg, const void* d_bitstream, uint64_t n_bytes,
+                       const uint64_t* d_lane_offsets, const void* d_pred, const void* d_tables,
+                       const uint8_t* d_bins, void* d_target_out, uint32_t* d_status, void* stream) {
   Geo g;
   int st = make_geo(p, &g);
   if (st != SKV_OK) return st;
@@ -1624,14 +1737,87 @@ int skv_decode(const skv_params* p, const void* d_bitstream, uint64_t n_bytes, c
   int blocks, threads;
   codec_grid(g.n_chunks, &blocks, &threads, kCodecThreads);
   const int smem_bytes = (int)(kDecTabBytes + (uint32_t)threads * kRingStride);
-  if (g.esz == 1) {
-    if ((st = set_smem(k_decode_kv<1>, kDecTabBytes + kCodecThreads * kRingStride)) != SKV_OK) return st;
-    k_decode_kv<1><<<blocks, threads, smem_bytes, s>>>(a);
+  const uint32_t smax = kDecTabBytes + kCodecThreads * kRingStride;
+  if (pg) a.pg = *pg;
+  if (g.esz == 1 && !pg) {
+    if ((st = set_smem(k_decode_kv<1, false>, smax)) != SKV_OK) return st;
+    k_decode_kv<1, false><<<blocks, threads, smem_bytes, s>>>(a);
+  } else if (g.esz == 1) {
+    if ((st = set_smem(k_decode_kv<1, true>, smax)) != SKV_OK) return st;
+    k_decode_kv<1, true><<<blocks, threads, smem_bytes, s>>>(a);
+  } else if (!pg) {
+    if ((st = set_smem(k_decode_kv<2, false>, smax)) != SKV_OK) return st;
+    k_decode_kv<2, false><<<blocks, threads, smem_bytes, s>>>(a);
   } else {
-    if ((st = set_smem(k_decode_kv<2>, kDecTabBytes + kCodecThreads * kRingStride)) != SKV_OK) return st;
-    k_decode_kv<2><<<blocks, threads, smem_bytes, s>>>(a);
+    if ((st = set_smem(k_decode_kv<2, true>, smax)) != SKV_OK) return st;
+    k_decode_kv<2, true><<<blocks, threads, smem_bytes, s>>>(a);
   }
   return launch_check();
+}
+
+int skv_encode(const skv_params* p, const void* d_target, const void* d_pred, const void* d_tables,
+               const uint8_t* d_bins, void* d_bitstream, uint64_t cap_bytes, uint64_t* d_lane_offsets,
+               void* d_workspace, uint64_t workspace_bytes, uint32_t* d_status, uint64_t* h_total_bytes,
+               void* stream) {
+  return encode_impl(p, nullptr, d_target, d_pred, d_tables, d_bins, d_bitstream, cap_bytes, d_lane_offsets,
+                     d_workspace, workspace_bytes, d_status, h_total_bytes, stream);
+}
+
+int skv_decode(const skv_params* p, const void* d_bitstream, uint64_t n_bytes, const uint64_t* d_lane_offsets,
+               const void* d_pred, const void* d_tables, const uint8_t* d_bins, void* d_target_out,
+               uint32_t* d_status, void* stream) {
+  return decode_impl(p, nullptr, d_bitstream, n_bytes, d_lane_offsets, d_pred, d_tables, d_bins, d_target_out,
+                     d_status, stream);
+}
+
+// Paged pools: checks the layout against the parameters (host only).
+static int paged_args(const skv_params* p, const skv_paged_layout* L, Paged* pg) {
+  Geo g;
+  int st = make_geo(p, &g);
+  if (st != SKV_OK) return st;
+  if (g.dtype == SKV_COEF_I16) return SKV_ERR_UNSUPPORTED;
+  if (!L || !L->d_block_table || ((uintptr_t)L->d_block_table & 3) || L->n_blocks == 0 || L->block_tokens == 0 ||
+      (L->block_tokens & (L->block_tokens - 1)) != 0)
+    return SKV_ERR_INVALID_ARG;
+  uint32_t shift = 0;
+  while ((1u << shift) < L->block_tokens) ++shift;
+  pg->bt = L->d_block_table;
+  pg->n_blocks = L->n_blocks;
+  pg->shift = shift;
+  pg->H = p->n_heads;
+  return SKV_OK;
+}
+
+int skv_calibrate_paged(const skv_params* p, const skv_paged_layout* layout, const void* d_target_pool,
+                        const void* d_pred_pool, uint8_t* d_bins, uint32_t* d_sum_abs, uint32_t* d_hist,
+                        uint32_t* d_status, void* stream) {
+  Paged pg;
+  int st = paged_args(p, layout, &pg);
+  if (st != SKV_OK) return st;
+  if (!d_status || ((uintptr_t)d_status & 3)) return SKV_ERR_INVALID_ARG;
+  return calibrate_impl(p, &pg, d_status, d_target_pool, d_pred_pool, d_bins, d_sum_abs, d_hist, stream);
+}
+
+int skv_encode_paged(const skv_params* p, const skv_paged_layout* layout, const void* d_target_pool,
+                     const void* d_pred_pool, const void* d_tables, const uint8_t* d_bins, void* d_bitstream,
+                     uint64_t cap_bytes, uint64_t* d_lane_offsets, void* d_workspace, uint64_t workspace_bytes,
+                     uint32_t* d_status, uint64_t* h_total_bytes, void* stream) {
+  Paged pg;
+  int st = paged_args(p, layout, &pg);
+  if (st != SKV_OK) return st;
+  return encode_impl(p, &pg, d_target_pool, d_pred_pool, d_tables, d_bins, d_bitstream, cap_bytes, d_lane_offsets,
+                     d_workspace, workspace_bytes, d_status, h_total_bytes, stream);
+}
+
+int skv_decode_paged(const skv_params* p, const skv_paged_layout* layout, const void* d_bitstream,
+                     uint64_t n_bytes, const uint64_t* d_lane_offsets, const void* d_pred_pool,
+                     const void* d_tables, const uint8_t* d_bins, void* d_target_pool_out, uint32_t* d_status,
+                     void* stream) {
+  Paged pg;
+  int st = paged_args(p, layout, &pg);
+  if (st != SKV_OK) return st;
+  return decode_impl(p, &pg, d_bitstream, n_bytes, d_lane_offsets, d_pred_pool, d_tables, d_bins,
+                     d_target_pool_out, d_status, stream);
 }
 
 // Scratch of skv_encode_noalloc: a file-scope device array, so the call never
@@ -1695,7 +1881,7 @@ int skv_read_status(const uint32_t* d_status, void* stream) {
   if (v & SKV_FLAG_CORRUPT) return SKV_ERR_CORRUPT;
   if (v & SKV_FLAG_CAPACITY) return SKV_ERR_CAPACITY;
   if (v & SKV_FLAG_TIMEOUT) return SKV_ERR_TIMEOUT;
-  if (v & SKV_FLAG_BAD_BIN) return SKV_ERR_INVALID_ARG;
+  if (v & (SKV_FLAG_BAD_BIN | SKV_FLAG_BAD_BLOCK)) return SKV_ERR_INVALID_ARG;
   return SKV_OK;
 }
 

@@ -37,6 +37,15 @@ class skv_params(C.Structure):
                 ("n_calib", C.c_uint32), ("reserved", C.c_uint32)]
 
 
+class skv_paged_layout(C.Structure):
+    _fields_ = [("d_block_table", C.c_void_p), ("n_blocks", C.c_uint32), ("block_tokens", C.c_uint32)]
+
+
+def paged_layout(block_table, n_blocks: int, block_tokens: int) -> skv_paged_layout:
+    """layout of paged pools; block_table: a uint32-valued device tensor (int32 storage)"""
+    return skv_paged_layout(_ptr(block_table), n_blocks, block_tokens)
+
+
 def kv_params(dtype, n_layers, n_kv, n_heads, head_dim, n_tokens, lane_syms, n_calib=256) -> skv_params:
     return skv_params(1, dtype, n_layers, n_kv, n_heads, head_dim, n_tokens, 0, lane_syms, n_calib, 0)
 
@@ -54,6 +63,7 @@ def params_for(w) -> skv_params:
 
 _lib = None
 _P = C.POINTER(skv_params)
+_PL = C.POINTER(skv_paged_layout)
 _SIGS = {
     "skv_status_string": (C.c_char_p, [C.c_int]),
     "skv_check_params": (C.c_int, [_P]),
@@ -76,6 +86,13 @@ _SIGS = {
     "skv_selftest_lookback": (C.c_int, [C.c_void_p, C.c_uint32, C.c_uint32, C.c_uint32, C.c_void_p, C.c_void_p,
                                         C.c_void_p]),
     "skv_read_status": (C.c_int, [C.c_void_p, C.c_void_p]),
+    "skv_calibrate_paged": (C.c_int, [_P, _PL, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                      C.c_void_p, C.c_void_p]),
+    "skv_encode_paged": (C.c_int, [_P, _PL, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                   C.c_uint64, C.c_void_p, C.c_void_p, C.c_uint64, C.c_void_p, C.c_void_p,
+                                   C.c_void_p]),
+    "skv_decode_paged": (C.c_int, [_P, _PL, C.c_void_p, C.c_uint64, C.c_void_p, C.c_void_p, C.c_void_p,
+                                   C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
 }
 
 
@@ -186,6 +203,31 @@ def skv_selftest_lookback(state, n_chunks, missing_chunk, max_spins, excl, statu
 
 def skv_read_status(status, stream=None) -> int:
     return lib().skv_read_status(_ptr(status), _stream(stream))
+
+
+# --- paged pools (same names as the C ABI) -----------------------------------------------------
+def skv_calibrate_paged(p, layout, target_pool, pred_pool, bins, status, sum_abs=None, hist=None,
+                        stream=None) -> int:
+    return lib().skv_calibrate_paged(C.byref(p), C.byref(layout), _ptr(target_pool), _ptr(pred_pool), _ptr(bins),
+                                     _ptr(sum_abs), _ptr(hist), _ptr(status), _stream(stream))
+
+
+def skv_encode_paged(p, layout, target_pool, pred_pool, tables, bins, bitstream, cap_bytes, lane_offsets,
+                     workspace, workspace_bytes, status, want_total=True, stream=None):
+    """Returns (status_code, total_bytes or None)."""
+    tot = C.c_uint64(0)
+    st = lib().skv_encode_paged(C.byref(p), C.byref(layout), _ptr(target_pool), _ptr(pred_pool), _ptr(tables),
+                                _ptr(bins), _ptr(bitstream), cap_bytes, _ptr(lane_offsets), _ptr(workspace),
+                                workspace_bytes, _ptr(status), C.byref(tot) if want_total else None,
+                                _stream(stream))
+    return st, (tot.value if want_total else None)
+
+
+def skv_decode_paged(p, layout, bitstream, n_bytes, lane_offsets, pred_pool, tables, bins, target_pool_out,
+                     status, stream=None) -> int:
+    return lib().skv_decode_paged(C.byref(p), C.byref(layout), _ptr(bitstream), n_bytes, _ptr(lane_offsets),
+                                  _ptr(pred_pool), _ptr(tables), _ptr(bins), _ptr(target_pool_out), _ptr(status),
+                                  _stream(stream))
 
 
 # --- convenience: device buffers from torch, the calls above, errors raised --------------------

@@ -171,3 +171,29 @@ def gen_workload(w: Workload, device="cpu"):
         return q, mu, beta
     t, p = gen_kv(w, device)
     return t, p, p
+
+
+def to_paged(target, pred, block_tokens: int, spare_blocks: int = 3, seed: int = 0):
+    """Copies dense caches [layer][kv][head][token][head_dim] into paged pools
+    [layer][kv][n_blocks][block_tokens][head][head_dim] under a seeded random
+    block table: the token blocks go to a random permutation of the pool's
+    blocks, `spare_blocks` blocks stay unused, and rows past the last token are
+    zero.  Returns (target_pool, pred_pool, block_table (int32 holding u32
+    block indices), n_blocks)."""
+    L, KV, H, T, D = target.shape
+    B = block_tokens
+    ntb = -(-T // B)
+    n_blocks = ntb + spare_blocks
+    g = torch.Generator().manual_seed(BASE_SEED * 7 + seed)
+    perm = torch.randperm(n_blocks, generator=g)[:ntb]
+
+    def pack(x):
+        xt = x.permute(0, 1, 3, 2, 4)                     # [L][kv][T][H][D]
+        pad = ntb * B - T
+        if pad:
+            xt = torch.cat([xt, torch.zeros((L, KV, pad, H, D), dtype=x.dtype, device=x.device)], dim=2)
+        pool = torch.zeros((L, KV, n_blocks, B, H, D), dtype=x.dtype, device=x.device)
+        pool[:, :, perm.to(x.device)] = xt.reshape(L, KV, ntb, B, H, D)
+        return pool
+
+    return pack(target), pack(pred), perm.to(torch.int32).to(target.device), n_blocks

@@ -71,3 +71,27 @@ def test_null_arguments_rejected_without_gpu(lib):
     st, _ = native.skv_encode(p, None, None, None, None, None, 0, None, None, 0, None, stream=0)
     assert st == native.SKV_ERR_INVALID_ARG
     assert native.skv_read_status(None, stream=0) == native.SKV_ERR_INVALID_ARG
+
+
+def test_paged_layout_rejected_without_gpu(lib):
+    """every malformed paged layout is refused before anything touches the GPU"""
+    p = native.kv_params(1, 1, 2, 8, 128, 100, 1024)
+    fake = 1 << 20        # never dereferenced: the layout check fails first
+    bad = [native.skv_paged_layout(None, 4, 16),          # no block table
+           native.skv_paged_layout(fake + 2, 4, 16),      # table not 4-byte aligned
+           native.skv_paged_layout(fake, 0, 16),          # no blocks
+           native.skv_paged_layout(fake, 4, 0),           # empty blocks
+           native.skv_paged_layout(fake, 4, 24)]          # not a power of two
+    for lay in bad:
+        assert native.skv_calibrate_paged(p, lay, fake, fake, fake, fake, stream=0) == native.SKV_ERR_INVALID_ARG
+        st, _ = native.skv_encode_paged(p, lay, fake, fake, fake, fake, fake, 16, fake, fake, 1 << 30, fake,
+                                        stream=0)
+        assert st == native.SKV_ERR_INVALID_ARG
+        assert native.skv_decode_paged(p, lay, fake, 16, fake, fake, fake, fake, fake, fake,
+                                       stream=0) == native.SKV_ERR_INVALID_ARG
+    c = native.coef_params(4, 16, 8)
+    good = native.skv_paged_layout(fake, 4, 16)
+    st, _ = native.skv_encode_paged(c, good, fake, fake, fake, fake, fake, 16, fake, fake, 1 << 30, fake, stream=0)
+    assert st == native.SKV_ERR_UNSUPPORTED
+    # a null status word is refused by the paged calibration before any launch
+    assert native.skv_calibrate_paged(p, good, fake, fake, fake, None, stream=0) == native.SKV_ERR_INVALID_ARG
