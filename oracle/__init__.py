@@ -42,12 +42,12 @@ class Params(C.Structure):
     _fields_ = [("version", C.c_uint32), ("dtype", C.c_uint32), ("n_layers", C.c_uint32),
                 ("n_kv", C.c_uint32), ("n_heads", C.c_uint32), ("head_dim", C.c_uint32),
                 ("n_tokens", C.c_uint64), ("n_coef", C.c_uint32), ("lane_syms", C.c_uint32),
-                ("n_calib", C.c_uint32), ("reserved", C.c_uint32)]
+                ("n_calib", C.c_uint32), ("model", C.c_uint32)]
 
 
 def kv_params(dtype: int, n_layers: int, n_kv: int, n_heads: int, head_dim: int,
-              n_tokens: int, lane_syms: int, n_calib: int = 256) -> Params:
-    return Params(1, dtype, n_layers, n_kv, n_heads, head_dim, n_tokens, 0, lane_syms, n_calib, 0)
+              n_tokens: int, lane_syms: int, n_calib: int = 256, model: int = 0) -> Params:
+    return Params(1, dtype, n_layers, n_kv, n_heads, head_dim, n_tokens, 0, lane_syms, n_calib, model)
 
 
 def coef_params(n_tokens: int, n_coef: int, lane_syms: int) -> Params:
@@ -67,6 +67,7 @@ def lib():
         sig = {
             "or_ordinal": (u32, [u32, u32]), "or_ordinal_inv": (u32, [u32, u32]),
             "or_bin_from_q": (u32, [u64, u32]), "or_beta_q": (u64, [u32, u32]),
+            "or_bin_ext": (u32, [u64]), "or_model1_table": (u32, [u32, u32]),
             "or_tau_q": (u64, [u64]), "or_power_chain": (None, [u64, vp]),
             "or_masses": (None, [u32, u32, u32, vp]),
             "or_build_table": (None, [u32, u32, u32, vp, vp]),

@@ -72,7 +72,9 @@ typedef struct {
   uint32_t n_coef;    /* COEF: layout [token][coef]                         */
   uint32_t lane_syms; /* K: positions per lane; a chunk is 32*K positions    */
   uint32_t n_calib;   /* calibration tokens per channel                      */
-  uint32_t reserved;
+  uint32_t model;     /* residual model: 0 per-channel scale bins, 1 (FP8)  */
+                      /* per-channel scale normalised by the prediction's   */
+                      /* exponent (see O3b)                                  */
 } or_params;
 
 /* ------------------------------------------------------------------------ */
@@ -123,6 +125,7 @@ uint64_t or_max_lane_words(const or_params *p) {
 
 int or_check_params(const or_params *p) {
   if (p->dtype != OR_FP8 && p->dtype != OR_BF16 && p->dtype != OR_COEF) return OR_ERR_ARG;
+  if (p->model > 1u || (p->model == 1u && p->dtype != OR_FP8)) return OR_ERR_ARG;
   if (p->lane_syms == 0 || (p->lane_syms % or_group(p)) != 0) return OR_ERR_ARG;
   if (p->dtype != OR_COEF) {
     if (p->head_dim == 0 || (p->head_dim % or_group(p)) != 0) return OR_ERR_ARG;
@@ -175,6 +178,32 @@ uint32_t or_bin_from_q(uint64_t q, uint32_t sub) {
   return sub * (pw - 13u) + (uint32_t)((q >> (pw - sb)) & (sub - 1u));
 }
 
+/* O3b: residual model 1 (FP8 only).  [SKV] names "more refined residual
+ * models" as the next step; READING: ordinals are evenly spaced in bit
+ * patterns, so a fixed value-space error spans 2^-e as many ordinals when the
+ * prediction's exponent field e = (bits >> 3) & 15 is one higher.  The
+ * channel's scale is therefore fitted on |r| 2^e (the scale at exponent 0),
+ * S'_c = sum |r| 2^e over the calibration tokens, q_c = floor(S'_c 2^16 / N),
+ * stored as its bin on the log grid extended upward without a cap (the base
+ * bin; q below 2^13 -> 0).  A position whose prediction has exponent e uses
+ * the table of the scale (base scale) / 2^e: the bin of the base bin's lower
+ * edge shifted down e octaves. */
+uint32_t or_bin_ext(uint64_t q) {
+  uint32_t pw = 0;
+  if (q < (1ull << 13)) return 0;
+  while ((q >> (pw + 1u)) != 0) pw++;
+  return 4u * (pw - 13u) + (uint32_t)((q >> (pw - 2u)) & 3u);
+}
+/* lower edge (Q16) of base bin b = 4 (p - 13) + j: leading one at p, j below */
+static uint64_t bin_ext_lower_q(uint32_t b) {
+  uint32_t pw = 13u + b / 4u, j = b % 4u;
+  if (pw > 61u) return UINT64_MAX;   /* beyond 2^62: above every table at any e <= 15 */
+  return (uint64_t)(4u + j) << (pw - 2u);
+}
+uint32_t or_model1_table(uint32_t base, uint32_t e) {
+  return or_bin_from_q(bin_ext_lower_q(base) >> e, 4u);
+}
+
 static uint32_t load_bits(const void *base, uint64_t idx, uint32_t esz) {
   if (esz == 1) return ((const uint8_t *)base)[idx];
   return ((const uint16_t *)base)[idx];
@@ -206,17 +235,19 @@ int or_calibrate(const or_params *p, const void *target, const void *pred,
       uint64_t c = s * D + d, S = 0;
       for (uint64_t t = 0; t < nc; t++) {
         uint64_t idx = (s * T + t) * D + d;
+        uint32_t pb = load_bits(pred, idx, esz);
         int64_t r = (int64_t)or_ordinal(load_bits(target, idx, esz), width) -
-                    (int64_t)or_ordinal(load_bits(pred, idx, esz), width);
-        S += (uint64_t)(r < 0 ? -r : r);
+                    (int64_t)or_ordinal(pb, width);
+        uint64_t a = (uint64_t)(r < 0 ? -r : r);
+        S += p->model == 1u ? a << ((pb >> 3) & 15u) : a;
         if (hist) {
           uint32_t sym = (r >= -RMAX && r <= RMAX) ? (uint32_t)(r + RMAX) : ESC;
           hist[c * NSYM + sym]++;
         }
       }
-      if (sum_abs) sum_abs[c] = (uint32_t)S;
+      if (sum_abs) sum_abs[c] = S > 0xFFFFFFFFull ? 0xFFFFFFFFu : (uint32_t)S;
       uint64_t q = nc ? (S << 16) / nc : 0;     /* floor(S * 2^16 / N) */
-      bins[c] = (uint8_t)or_bin_from_q(q, 4u);
+      bins[c] = (uint8_t)(p->model == 1u ? or_bin_ext(q) : or_bin_from_q(q, 4u));
     }
   }
   return OR_OK;
@@ -379,9 +410,9 @@ static void position_symbol(const or_params *p, uint64_t slice, uint64_t pos_in_
   }
   uint32_t esz = elem_bytes(p), width = 8u * esz;
   uint64_t c = slice * p->head_dim + pos_in_slice % p->head_dim;
-  o->table = bins[c];
-  int64_t r = (int64_t)or_ordinal(load_bits(tgt, idx, esz), width) -
-              (int64_t)or_ordinal(load_bits(prd, idx, esz), width);
+  uint32_t pb = load_bits(prd, idx, esz);
+  o->table = p->model == 1u ? or_model1_table(bins[c], (pb >> 3) & 15u) : bins[c];
+  int64_t r = (int64_t)or_ordinal(load_bits(tgt, idx, esz), width) - (int64_t)or_ordinal(pb, width);
   residual_symbol(r, width, o);
 }
 
@@ -600,7 +631,8 @@ int or_decode_chunk(const or_params *p, uint64_t chunk, const uint16_t *freq_all
         coef_mean(((const float *)prd)[idx], &m, &f);
         table = 16u * bins[c] + f;
       } else {
-        table = bins[ch.slice * p->head_dim + pis % p->head_dim];
+        uint32_t b = bins[ch.slice * p->head_dim + pis % p->head_dim];
+        table = p->model == 1u ? or_model1_table(b, (load_bits(prd, idx, esz) >> 3) & 15u) : b;
       }
       const uint16_t *fr = freq_all + (uint64_t)table * NSYM;
       const uint16_t *cm = cum_all + (uint64_t)table * (NSYM + 1);
