@@ -241,7 +241,7 @@ def main_ours(args):
     w = synth.WORKLOADS[args.workload]
     if args.layers:
         w = w.scaled(n_layers=args.layers)
-    p = native.params_for(w)
+    p = native.params_for(w, model=args.model)
     sz = native.sizes(p)
     stream = torch.cuda.current_stream(dev)
 
@@ -321,6 +321,7 @@ def main_ours(args):
         "vs_baseline": None, "dtype": "u8" if w.dtype == synth.FP8 else ("u16" if w.dtype == synth.BF16 else "i16"),
         "data": "synthetic",
         "config": {"workload": w.name, "shape": list(w.shape()), "lane_syms": w.lane_syms,
+                   "residual_model": ["per-channel scale", "exponent-normalised scale"][args.model],
                    "l2": "inputs larger than L2 (no flush)",
                    "step": "calibrate + build_tables + encode + decode"},
         "phases_ms": phase,
@@ -467,6 +468,8 @@ def main():
     ap.add_argument("--cap-frac", type=float, default=0.6, help="bitstream buffer / raw bytes")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--paged", type=int, default=0, help="also time paged pools with this many tokens per block")
+    ap.add_argument("--model", type=int, default=0, choices=[0, 1],
+                    help="residual model: 0 per-channel scale (default), 1 exponent-normalised (FP8)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

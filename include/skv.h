@@ -117,8 +117,25 @@ typedef struct {
   uint32_t lane_syms; /* positions per lane (chunk = 32 lanes); a multiple of
                          the group size (16 FP8, 8 otherwise), at most 65536    */
   uint32_t n_calib;   /* KV only: calibration tokens per channel (<= 65536)     */
-  uint32_t reserved;  /* must be 0                                              */
+  uint32_t model;     /* residual model: 0 = one Laplace scale bin per channel;
+                         1 (FP8 only) = the channel's scale normalised by the
+                         prediction's exponent (see SKV_MODEL_EXPONENT)        */
 } skv_params;
+
+/* Residual models ([SKV] names more refined residual models as the next
+ * step; the plain reading below is this library's).
+ * SKV_MODEL_CHANNEL: calibration stores per channel the bin (0..31) of the
+ *   Laplace scale fitted on |r|, and every position uses that table.
+ * SKV_MODEL_EXPONENT (FP8): ordinals are evenly spaced in bit patterns, so
+ *   one value-space error spans half as many ordinals per step up of the
+ *   prediction's exponent field e = (pred_bits >> 3) & 15.  Calibration fits
+ *   the scale on |r| * 2^e (S_c = sum of |r| 2^e, q = floor(S_c 2^16 / N))
+ *   and stores its base bin on the scale grid extended upward (4 bins per
+ *   octave, 0 below 1/8, no cap); a position then uses table
+ *   min(max(base - 4 e, 0), 31).  d_sum_abs receives S_c (saturated at
+ *   2^32 - 1). */
+#define SKV_MODEL_CHANNEL 0u
+#define SKV_MODEL_EXPONENT 1u
 
 /* Text for a status code (static storage). */
 const char* skv_status_string(int status);

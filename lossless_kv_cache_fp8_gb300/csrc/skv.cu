@@ -74,16 +74,18 @@ constexpr int kScanPerBlock = 4096;       // lanes per scan block (256 threads x
 // Host-side geometry
 // ---------------------------------------------------------------------------
 struct Geo {
-  uint32_t dtype, esz, group, raw_bytes, K, D, C, n_tables, sub;
+  uint32_t dtype, esz, group, raw_bytes, K, D, C, n_tables, sub, model;
   uint64_t T, n_slices, slice_pos, cps, n_chunks, n_lanes, n_channels, n_positions;
   uint64_t slot_words;
 };
 
 int make_geo(const skv_params* p, Geo* g) {
   if (!p || !g) return SKV_ERR_INVALID_ARG;
-  if (p->version != SKV_PARAMS_VERSION || p->reserved != 0) return SKV_ERR_INVALID_ARG;
+  if (p->version != SKV_PARAMS_VERSION || p->model > SKV_MODEL_EXPONENT) return SKV_ERR_INVALID_ARG;
+  if (p->model == SKV_MODEL_EXPONENT && p->dtype != SKV_FP8_E4M3) return SKV_ERR_UNSUPPORTED;
   memset(g, 0, sizeof(*g));
   g->dtype = p->dtype;
+  g->model = p->model;
   if (p->dtype == SKV_FP8_E4M3) { g->esz = 1; g->group = 16; g->raw_bytes = 1; }
   else if (p->dtype == SKV_BF16) { g->esz = 2; g->group = 8; g->raw_bytes = 2; }
   else if (p->dtype == SKV_COEF_I16) { g->esz = 2; g->group = 8; g->raw_bytes = 2; }
@@ -205,6 +207,39 @@ __device__ __forceinline__ uint32_t bin_from_q(uint64_t q, uint32_t sub) {
   if (q >= (1ull << 21)) return 8 * sub - 1;
   const uint32_t pw = 63 - __clzll((long long)q);
   return sub * (pw - 13) + (uint32_t)((q >> (pw - sb)) & (sub - 1));
+}
+
+// base bin of the exponent model: the same grid extended upward without a cap
+// (0 below 1/8); a position with prediction exponent e uses table
+// min(max(base - 4 e, 0), 31)
+__device__ __forceinline__ uint32_t bin_ext(uint64_t q) {
+  if (q < (1ull << 13)) return 0;
+  const uint32_t pw = 63 - __clzll((long long)q);
+  return 4 * (pw - 13) + (uint32_t)((q >> (pw - 2)) & 3u);
+}
+__device__ __forceinline__ uint32_t vmin_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// Exponent model (FP8): table byte offsets of a group's 16 positions from the
+// lane's base bins (bw, four words of bytes) and the group's raw prediction
+// words, two positions at a time in 16-bit lanes:
+// base - min(base, 4 e) = max(base - 4 e, 0), then min with 31.
+__device__ __forceinline__ void model_exp_word(uint32_t b, uint32_t w, uint32_t stride, uint32_t* t4) {
+  const uint32_t e_ev = (w >> 1) & 0x003C003Cu, e_od = (w >> 9) & 0x003C003Cu;   // 4 e of bytes 0|2, 1|3
+  const uint32_t b_ev = b & 0x00FF00FFu, b_od = (b >> 8) & 0x00FF00FFu;
+  const uint32_t i_ev = vmin_u16x2(b_ev - vmin_u16x2(b_ev, e_ev), 0x001F001Fu);
+  const uint32_t i_od = vmin_u16x2(b_od - vmin_u16x2(b_od, e_od), 0x001F001Fu);
+  t4[0] = (i_ev & 0xFFFFu) * stride;
+  t4[1] = (i_od & 0xFFFFu) * stride;
+  t4[2] = (i_ev >> 16) * stride;
+  t4[3] = (i_od >> 16) * stride;
+}
+__device__ __forceinline__ void model_exp_tables(const uint32_t* bw, const uint4& praw, uint32_t stride,
+                                                 uint32_t* tb) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) model_exp_word(bw[k], word_of(praw, k), stride, tb + 4 * k);
 }
 
 // ---- shared-memory access by byte offset into the dynamic shared array -----
@@ -570,7 +605,7 @@ template <int ESZ, bool PAGED>
 __global__ void __launch_bounds__(256) k_calibrate_kv(const uint8_t* tgt, const uint8_t* prd,
                                                       uint8_t* bins, uint32_t* sum_abs,
                                                       uint32_t* hist, uint64_t T, uint32_t D,
-                                                      uint32_t nc, Paged pg, uint32_t* status) {
+                                                      uint32_t nc, Paged pg, uint32_t* status, uint32_t model) {
   constexpr int G = 16 / ESZ;
   __shared__ unsigned long long S[512];
   const uint64_t slice = blockIdx.x;
@@ -579,7 +614,7 @@ __global__ void __launch_bounds__(256) k_calibrate_kv(const uint8_t* tgt, const 
   const uint32_t cg = tid % nv, tph = tid / nv, nph = blockDim.x / nv;
   for (uint32_t d = tid; d < D; d += blockDim.x) S[d] = 0;
   __syncthreads();
-  uint32_t acc[G];
+  unsigned long long acc[G];   // model 1 adds |r| 2^e: up to 2^23 per token
 #pragma unroll
   for (int e = 0; e < G; ++e) acc[e] = 0;
   const uint64_t base = slice * T * D;          // element index of the slice
@@ -597,7 +632,8 @@ __global__ void __launch_bounds__(256) k_calibrate_kv(const uint8_t* tgt, const 
           const uint32_t sh = 8 * ESZ * h, mk = ESZ == 1 ? 0xFFu : 0xFFFFu;
           const int r = (int)((a >> sh) & mk) - (int)((b >> sh) & mk);
           const int e = k * (4 / ESZ) + h;
-          acc[e] += (uint32_t)(r < 0 ? -r : r);
+          const uint32_t ex = model ? (word_of(pv, k) >> (sh + 3)) & 15u : 0u;   // prediction's exponent field
+          acc[e] += (unsigned long long)(uint32_t)(r < 0 ? -r : r) << ex;
           if (hist) {
             const uint32_t sym = (r >= -127 && r <= 127) ? (uint32_t)(r + 127) : 255u;
             atomicAdd(&hist[((slice * D) + (uint64_t)cg * G + e) * 256 + sym], 1u);
@@ -609,20 +645,20 @@ __global__ void __launch_bounds__(256) k_calibrate_kv(const uint8_t* tgt, const 
   // lanes tid, tid + nv, ... of one warp share a channel group
 #pragma unroll
   for (int e = 0; e < G; ++e) {
-    uint32_t v = acc[e];
+    unsigned long long v = acc[e];
     for (uint32_t o = nv; o < 32; o <<= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
     acc[e] = v;
   }
   if ((tid & 31) < nv && tph < nph) {
 #pragma unroll
-    for (int e = 0; e < G; ++e) atomicAdd(&S[cg * G + e], (unsigned long long)acc[e]);
+    for (int e = 0; e < G; ++e) atomicAdd(&S[cg * G + e], acc[e]);
   }
   __syncthreads();
   for (uint32_t d = tid; d < D; d += blockDim.x) {
     const uint64_t sv = S[d];
     const uint64_t q = nc ? (sv << 16) / nc : 0;
-    bins[slice * D + d] = (uint8_t)bin_from_q(q, 4);
-    if (sum_abs) sum_abs[slice * D + d] = (uint32_t)sv;
+    bins[slice * D + d] = (uint8_t)(model ? bin_ext(q) : bin_from_q(q, 4));
+    if (sum_abs) sum_abs[slice * D + d] = sv > 0xFFFFFFFFull ? 0xFFFFFFFFu : (uint32_t)sv;
   }
 }
 
@@ -689,6 +725,12 @@ __device__ __forceinline__ void load_lane_tables(const CodecArgs& a, uint64_t sl
     tb[e] = b * stride;
   }
   if (bad) atomicOr(a.status, SKV_FLAG_BAD_BIN);
+}
+
+// exponent model: the lane's 16 base bins as four words of bytes
+__device__ __forceinline__ void load_lane_bases(const CodecArgs& a, uint64_t slice, uint32_t d0, uint32_t* bw) {
+  const uint4 v = *reinterpret_cast<const uint4*>(a.bins + slice * a.D + d0);
+  bw[0] = v.x; bw[1] = v.y; bw[2] = v.z; bw[3] = v.w;
 }
 
 // Flush the oldest complete 16-byte blocks of every lane's word buffer (the
@@ -871,7 +913,7 @@ __device__ __noinline__ void place_chunk(const CodecArgs& a, unsigned long long 
   __syncwarp();
 }
 
-template <int ESZ, bool PAGED>
+template <int ESZ, bool PAGED, bool MODEL>
 __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
   constexpr int G = 16 / ESZ;
   // Room the word buffer must have before a group: a symbol step emits at
@@ -917,8 +959,11 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
     const uint32_t n_groups = (uint32_t)(n_pos / G);
     const uint32_t n_g = lane < n_groups ? (n_groups - lane + 31) / 32 : 0;
     const int n_iter = (int)((n_groups + 31) / 32);            // warp-uniform (lane 0 has the most)
-    uint32_t tb[G];
-    load_lane_tables<ESZ>(a, slice, (lane * G) % a.D, kEncTabStride, tb);
+    // table offsets of the lane's positions: fixed per channel, or (exponent
+    // model) recomputed for every group from the base bins bw
+    uint32_t tb[G], bw[4];
+    if (MODEL) load_lane_bases(a, slice, (lane * G) % a.D, bw);
+    else load_lane_tables<ESZ>(a, slice, (lane * G) % a.D, kEncTabStride, tb);
     const uint64_t off = (slice * a.slice_pos + first) * ESZ + lane * 16;
     // byte offset of this lane's group k of the chunk in the caches
     const uint32_t tpi = 32u * G / a.D;   // tokens between a lane's consecutive groups
@@ -998,11 +1043,14 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
       if (__any_sync(act, esc)) {
         // rare: exact residuals per position, raw steps where one escapes
         if (__any_sync(act, buf_top - rp > kRoomEsc)) emit_flush_sync(act, buf_top, rp, gp);
+        uint32_t t4[4];
 #pragma unroll
         for (int e = G - 1; e >= 0; --e) {
           constexpr uint32_t mk = ESZ == 1 ? 0xFFu : 0xFFFFu;
           const uint32_t sh = ESZ == 1 ? 8 * (e & 3) : 16 * (e & 1);
           const int wi = ESZ == 1 ? (e >> 2) : (e >> 1);
+          if (MODEL && (e & 3) == 3) model_exp_word(bw[e >> 2], word_of(pc, e >> 2), kEncTabStride, t4);
+          const uint32_t tbe = MODEL ? t4[e & 3] : tb[e];
           const uint32_t ot = ESZ == 1 ? ord8x4(word_of(tc, wi)) : ord16x2(word_of(tc, wi));
           const uint32_t op = ESZ == 1 ? ord8x4(word_of(pc, wi)) : ord16x2(word_of(pc, wi));
           const int r = (int)((ot >> sh) & mk) - (int)((op >> sh) & mk);
@@ -1011,12 +1059,14 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
           const uint32_t raw = (uint32_t)r & mk;
           enc_raw_smem_if(x, rp, raw & 0xFFu, e_j);
           if (ESZ == 2) enc_raw_smem_if(x, rp, raw >> 8, e_j);
-          enc_step_smem(x, rp, lds_u64(tb[e] + (e_j ? 255u : sy) * 8u));
+          enc_step_smem(x, rp, lds_u64(tbe + (e_j ? 255u : sy) * 8u));
         }
       } else {
         if (__any_sync(act, buf_top - rp > kRoomPlain)) emit_flush_sync(act, buf_top, rp, gp);
+        uint32_t t4[4];
 #pragma unroll
         for (int e = G - 1; e >= 0; --e) {
+          if (MODEL && (e & 3) == 3) model_exp_word(bw[e >> 2], word_of(pc, e >> 2), kEncTabStride, t4);
           // byte offset of the entry: 8 * symbol (the upper lane's shift
           // also drops the lower lane, whose value is below 2^13)
           uint32_t so;
@@ -1026,7 +1076,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
           } else {
             so = ((e & 1) ? vo[e >> 1] : ve[e >> 1]) << 3;
           }
-          enc_step_smem(x, rp, lds_u64(tb[e] + so));
+          enc_step_smem(x, rp, lds_u64((MODEL ? t4[e & 3] : tb[e]) + so));
         }
       }
       tc = tn;
@@ -1101,7 +1151,7 @@ __device__ __forceinline__ void dec_exact(RingLane& L, uint32_t tbe, uint32_t pw
   sw += term << sh;
 }
 
-template <int ESZ, bool PAGED>
+template <int ESZ, bool PAGED, bool MODEL>
 __global__ void __launch_bounds__(kCodecThreads, 1) k_decode_kv(CodecArgs a) {
   constexpr int G = 16 / ESZ;
   constexpr int SUB = ESZ == 1 ? 8 : 4;   // at most 32 / 24 stream bytes between refills
@@ -1124,8 +1174,9 @@ __global__ void __launch_bounds__(kCodecThreads, 1) k_decode_kv(CodecArgs a) {
     const uint64_t n_pos = min(chunk_pos, a.slice_pos - first);
     const uint32_t n_groups = (uint32_t)(n_pos / G);
     const uint32_t n_g = lane < n_groups ? (n_groups - lane + 31) / 32 : 0;
-    uint32_t tb[G];
-    load_lane_tables<ESZ>(a, slice, (lane * G) % a.D, kDecTabStride, tb);
+    uint32_t tb[G], bw[4];
+    if (MODEL) load_lane_bases(a, slice, (lane * G) % a.D, bw);
+    else load_lane_tables<ESZ>(a, slice, (lane * G) % a.D, kDecTabStride, tb);
     const uint64_t g = chunk * kLanes + lane;
     uint64_t sa, sb;
     const bool ok = lane_span(a.offs, g, a.n_lanes, a.n_bytes, &sa, &sb);
@@ -1164,6 +1215,7 @@ __global__ void __launch_bounds__(kCodecThreads, 1) k_decode_kv(CodecArgs a) {
         bool ok;
         pn = ldg_stream(a.prd + goff(i + 1, btn1, ok));
       }
+      if (MODEL) model_exp_tables(bw, pc, kDecTabStride, tb);
       uint32_t pw[4], sw[4] = {0, 0, 0, 0};
 #pragma unroll
       for (int k = 0; k < 4; ++k) pw[k] = ESZ == 1 ? ord8x4(word_of(pc, k)) : ord16x2(word_of(pc, k));
@@ -1555,11 +1607,11 @@ static int calibrate_impl(const skv_params* p, const Paged* pg, uint32_t* d_stat
   const Paged dense = {nullptr, 0, 0, 1};
   const unsigned nb = (unsigned)g.n_slices;
   if (g.esz == 1) {
-    if (pg) k_calibrate_kv<1, true><<<nb, 256, 0, s>>>(t8, p8, d_bins, d_sum_abs, d_hist, g.T, g.D, nc, *pg, d_status);
-    else k_calibrate_kv<1, false><<<nb, 256, 0, s>>>(t8, p8, d_bins, d_sum_abs, d_hist, g.T, g.D, nc, dense, nullptr);
+    if (pg) k_calibrate_kv<1, true><<<nb, 256, 0, s>>>(t8, p8, d_bins, d_sum_abs, d_hist, g.T, g.D, nc, *pg, d_status, g.model);
+    else k_calibrate_kv<1, false><<<nb, 256, 0, s>>>(t8, p8, d_bins, d_sum_abs, d_hist, g.T, g.D, nc, dense, nullptr, g.model);
   } else {
-    if (pg) k_calibrate_kv<2, true><<<nb, 256, 0, s>>>(t8, p8, d_bins, d_sum_abs, d_hist, g.T, g.D, nc, *pg, d_status);
-    else k_calibrate_kv<2, false><<<nb, 256, 0, s>>>(t8, p8, d_bins, d_sum_abs, d_hist, g.T, g.D, nc, dense, nullptr);
+    if (pg) k_calibrate_kv<2, true><<<nb, 256, 0, s>>>(t8, p8, d_bins, d_sum_abs, d_hist, g.T, g.D, nc, *pg, d_status, 0u);
+    else k_calibrate_kv<2, false><<<nb, 256, 0, s>>>(t8, p8, d_bins, d_sum_abs, d_hist, g.T, g.D, nc, dense, nullptr, 0u);
   }
   return launch_check();
 }
@@ -1640,19 +1692,15 @@ static int encode_impl(const skv_params* p, const Paged* pg, const void* d_targe
     const int smem_bytes = (int)(kEncTabBytes + (uint32_t)threads * kEmitBytes);
     const uint32_t smax = kEncTabBytes + kEncThreads * kEmitBytes;
     if (pg) a.pg = *pg;
-    if (g.esz == 1 && !pg) {
-      if ((st = set_smem(k_encode_kv<1, false>, smax)) != SKV_OK) return st;
-      k_encode_kv<1, false><<<blocks, threads, smem_bytes, s>>>(a);
-    } else if (g.esz == 1) {
-      if ((st = set_smem(k_encode_kv<1, true>, smax)) != SKV_OK) return st;
-      k_encode_kv<1, true><<<blocks, threads, smem_bytes, s>>>(a);
-    } else if (!pg) {
-      if ((st = set_smem(k_encode_kv<2, false>, smax)) != SKV_OK) return st;
-      k_encode_kv<2, false><<<blocks, threads, smem_bytes, s>>>(a);
-    } else {
-      if ((st = set_smem(k_encode_kv<2, true>, smax)) != SKV_OK) return st;
-      k_encode_kv<2, true><<<blocks, threads, smem_bytes, s>>>(a);
-    }
+    auto run = [&](auto kern) -> int {
+      int e = set_smem(kern, smax);
+      if (e == SKV_OK) kern<<<blocks, threads, smem_bytes, s>>>(a);
+      return e;
+    };
+    if (g.esz == 2) st = pg ? run(k_encode_kv<2, true, false>) : run(k_encode_kv<2, false, false>);
+    else if (g.model) st = pg ? run(k_encode_kv<1, true, true>) : run(k_encode_kv<1, false, true>);
+    else st = pg ? run(k_encode_kv<1, true, false>) : run(k_encode_kv<1, false, false>);
+    if (st != SKV_OK) return st;
     if ((st = launch_check()) != SKV_OK) return st;
     if (h_total_bytes) {
       uint64_t total = 0;
@@ -1739,19 +1787,15 @@ static int decode_impl(const skv_params* p, const Paged* pg, const void* d_bitst
   const int smem_bytes = (int)(kDecTabBytes + (uint32_t)threads * kRingStride);
   const uint32_t smax = kDecTabBytes + kCodecThreads * kRingStride;
   if (pg) a.pg = *pg;
-  if (g.esz == 1 && !pg) {
-    if ((st = set_smem(k_decode_kv<1, false>, smax)) != SKV_OK) return st;
-    k_decode_kv<1, false><<<blocks, threads, smem_bytes, s>>>(a);
-  } else if (g.esz == 1) {
-    if ((st = set_smem(k_decode_kv<1, true>, smax)) != SKV_OK) return st;
-    k_decode_kv<1, true><<<blocks, threads, smem_bytes, s>>>(a);
-  } else if (!pg) {
-    if ((st = set_smem(k_decode_kv<2, false>, smax)) != SKV_OK) return st;
-    k_decode_kv<2, false><<<blocks, threads, smem_bytes, s>>>(a);
-  } else {
-    if ((st = set_smem(k_decode_kv<2, true>, smax)) != SKV_OK) return st;
-    k_decode_kv<2, true><<<blocks, threads, smem_bytes, s>>>(a);
-  }
+  auto run = [&](auto kern) -> int {
+    int e = set_smem(kern, smax);
+    if (e == SKV_OK) kern<<<blocks, threads, smem_bytes, s>>>(a);
+    return e;
+  };
+  if (g.esz == 2) st = pg ? run(k_decode_kv<2, true, false>) : run(k_decode_kv<2, false, false>);
+  else if (g.model) st = pg ? run(k_decode_kv<1, true, true>) : run(k_decode_kv<1, false, true>);
+  else st = pg ? run(k_decode_kv<1, true, false>) : run(k_decode_kv<1, false, false>);
+  if (st != SKV_OK) return st;
   return launch_check();
 }
 

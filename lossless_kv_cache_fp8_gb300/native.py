@@ -34,7 +34,7 @@ class skv_params(C.Structure):
     _fields_ = [("version", C.c_uint32), ("dtype", C.c_uint32), ("n_layers", C.c_uint32),
                 ("n_kv", C.c_uint32), ("n_heads", C.c_uint32), ("head_dim", C.c_uint32),
                 ("n_tokens", C.c_uint64), ("n_coef", C.c_uint32), ("lane_syms", C.c_uint32),
-                ("n_calib", C.c_uint32), ("reserved", C.c_uint32)]
+                ("n_calib", C.c_uint32), ("model", C.c_uint32)]
 
 
 class skv_paged_layout(C.Structure):
@@ -46,19 +46,22 @@ def paged_layout(block_table, n_blocks: int, block_tokens: int) -> skv_paged_lay
     return skv_paged_layout(_ptr(block_table), n_blocks, block_tokens)
 
 
-def kv_params(dtype, n_layers, n_kv, n_heads, head_dim, n_tokens, lane_syms, n_calib=256) -> skv_params:
-    return skv_params(1, dtype, n_layers, n_kv, n_heads, head_dim, n_tokens, 0, lane_syms, n_calib, 0)
+SKV_MODEL_CHANNEL, SKV_MODEL_EXPONENT = 0, 1
+
+
+def kv_params(dtype, n_layers, n_kv, n_heads, head_dim, n_tokens, lane_syms, n_calib=256, model=0) -> skv_params:
+    return skv_params(1, dtype, n_layers, n_kv, n_heads, head_dim, n_tokens, 0, lane_syms, n_calib, model)
 
 
 def coef_params(n_tokens, n_coef, lane_syms) -> skv_params:
     return skv_params(1, SKV_COEF_I16, 0, 0, 0, 0, n_tokens, n_coef, lane_syms, 0, 0)
 
 
-def params_for(w) -> skv_params:
+def params_for(w, model: int = 0) -> skv_params:
     """skv_params of a synth.Workload"""
     if w.dtype == SKV_COEF_I16:
         return coef_params(w.n_tokens, w.n_coef, w.lane_syms)
-    return kv_params(w.dtype, w.n_layers, w.n_kv, w.n_heads, w.head_dim, w.n_tokens, w.lane_syms, w.n_calib)
+    return kv_params(w.dtype, w.n_layers, w.n_kv, w.n_heads, w.head_dim, w.n_tokens, w.lane_syms, w.n_calib, model)
 
 
 _lib = None

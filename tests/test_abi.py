@@ -95,3 +95,12 @@ def test_paged_layout_rejected_without_gpu(lib):
     assert st == native.SKV_ERR_UNSUPPORTED
     # a null status word is refused by the paged calibration before any launch
     assert native.skv_calibrate_paged(p, good, fake, fake, fake, None, stream=0) == native.SKV_ERR_INVALID_ARG
+
+
+def test_model_field_validated_without_gpu(lib):
+    p = native.kv_params(1, 1, 2, 8, 128, 100, 1024, model=native.SKV_MODEL_EXPONENT)
+    assert native.skv_check_params(p) == native.SKV_OK
+    p.model = 2
+    assert native.skv_check_params(p) == native.SKV_ERR_INVALID_ARG
+    b = native.kv_params(2, 1, 2, 8, 128, 100, 1024, model=native.SKV_MODEL_EXPONENT)
+    assert native.skv_check_params(b) == native.SKV_ERR_UNSUPPORTED
