@@ -197,3 +197,45 @@ def to_paged(target, pred, block_tokens: int, spare_blocks: int = 3, seed: int =
         return pool
 
     return pack(target), pack(pred), perm.to(torch.int32).to(target.device), n_blocks
+
+
+# ---- checkerboard context (the DCKV page's two-pass context model) --------------------------
+# The page's learned rank-1024 map is replaced by a seeded one: two integer factor
+# matrices with entries in [-8, 8].  The generator below uses them as a real-valued
+# linear map (no quantisation), so the coded data carries the structure a context
+# model can exploit; the coder's own integer arithmetic is not part of this module.
+CTX_RANK, CTX_SHIFT1, CTX_SHIFT2 = 1024, 6, 8
+
+
+def ctx_map(n_coef: int, rank: int = CTX_RANK, seed: int = 0):
+    """(V int8 [rank][n_coef], U int8 [n_coef][rank]), entries uniform in [-8, 8]"""
+    g = torch.Generator().manual_seed(BASE_SEED * 13 + seed)
+    V = torch.randint(-8, 9, (rank, n_coef), generator=g, dtype=torch.int32).to(torch.int8)
+    U = torch.randint(-8, 9, (n_coef, rank), generator=g, dtype=torch.int32).to(torch.int8)
+    return V, U
+
+
+def gen_coef_checkerboard(w: Workload, device="cpu", rank: int = CTX_RANK):
+    """Coefficient rows split by token parity.  Even rows are gen_coef's rows.
+    Odd row t (token 2t + 1) has mean mu_t + U V x_t / 2^(s1 + s2) / 16 (step
+    units), x_t = clamp(q_{2t} + q_{2t+2}, +-127) (a missing right neighbour is
+    0), and q = clamp(rint(mean + Laplace(0, beta_c)), +-32767) (switched-off
+    components 0).  Returns (q_even, q_odd, mu_even, mu_odd, beta, V, U)."""
+    assert w.dtype == COEF
+    q, mu, beta = gen_coef(w, device)
+    T, C = q.shape
+    V, U = ctx_map(C, rank)
+    q_even, mu_even, mu_odd = q[0::2].contiguous(), mu[0::2].contiguous(), mu[1::2].contiguous()
+    T_o = T // 2
+    right = torch.zeros((T_o, C), dtype=torch.int64, device=device)
+    n_r = min(T_o, q_even.shape[0] - 1)
+    right[:n_r] = q_even[1:1 + n_r].to(torch.int64)
+    x = (q_even[:T_o].to(torch.int64) + right).clamp_(-127, 127).to(torch.float64)
+    shift = (x @ V.to(device).to(torch.float64).T) @ U.to(device).to(torch.float64).T
+    shift = shift / float(1 << (CTX_SHIFT1 + CTX_SHIFT2)) / 16.0
+    gd = torch.Generator(device=device).manual_seed(w.seed * 1000003 + 11)
+    bd = beta.to(device)
+    noise = _laplace((T_o, C), bd, gd, device).to(torch.float64)
+    q_odd = torch.round(mu_odd.to(torch.float64) + shift + noise).clamp_(-32767, 32767).to(torch.int16)
+    q_odd[:, ~(beta >= 0.05).to(device)] = 0
+    return q_even, q_odd, mu_even, mu_odd, beta.to(device), V.to(device), U.to(device)

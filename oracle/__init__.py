@@ -68,6 +68,7 @@ def lib():
             "or_ordinal": (u32, [u32, u32]), "or_ordinal_inv": (u32, [u32, u32]),
             "or_bin_from_q": (u32, [u64, u32]), "or_beta_q": (u64, [u32, u32]),
             "or_bin_ext": (u32, [u64]), "or_model1_table": (u32, [u32, u32]),
+            "or_ctx_means": (i32, [u32, u32, vp, vp, u32, u32, vp, u64, vp, u64, vp]),
             "or_tau_q": (u64, [u64]), "or_power_chain": (None, [u64, vp]),
             "or_masses": (None, [u32, u32, u32, vp]),
             "or_build_table": (None, [u32, u32, u32, vp, vp]),
@@ -275,3 +276,18 @@ def rans_decode(prob_bits: int, freq, cum, words, n: int):
     out = np.zeros(max(n, 1), np.uint32)
     st = lib().or_rans_decode(prob_bits, _ptr(f), _ptr(c), len(f), _ptr(w), len(w), n, _ptr(out))
     return st, out[:n]
+
+
+def ctx_means(V, U, s1, s2, q_even, mu_odd):
+    """odd rows' context-shifted means (float32 [n_odd][C]) from the even rows"""
+    V = np.ascontiguousarray(V, np.int8)
+    U = np.ascontiguousarray(U, np.int8)
+    qe = np.ascontiguousarray(q_even, np.int16)
+    mo = np.ascontiguousarray(mu_odd, np.float32)
+    R, C = V.shape
+    out = np.zeros(mo.shape, np.float32)
+    st = lib().or_ctx_means(C, R, _ptr(V), _ptr(U), s1, s2, _ptr(qe), qe.shape[0], _ptr(mo), mo.shape[0],
+                            _ptr(out))
+    if st != OK:
+        raise ValueError(f"or_ctx_means status {st}")
+    return out

@@ -771,3 +771,54 @@ int or_symbols(const or_params *p, const uint8_t *bins, const void *target, cons
   }
   return OR_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Checkerboard context ([DCKV] how it differs): the coefficient rows are     */
+/* split by token parity; even rows are coded with the token-conditioned      */
+/* means alone, odd rows with means that also depend on the decoded rows on   */
+/* both sides through a rank-R linear map, so each parity decodes in one      */
+/* token-parallel pass.  READING (the page's map is learned; none is given):  */
+/* an integer map with factor matrices V [R][C], U [C][R] (int8), and         */
+/*   x   = clamp(q_even[t] + q_even[t+1], -127, 127)  (missing row -> 0)      */
+/*   g_r = clamp(floor((V x)_r / 2^s1), -127, 127)                            */
+/*   k_c = floor((U g)_c / 2^s2)               (context shift, 1/16 steps)    */
+/*   mu' = clamp(mu_q + k, +-(2^23 - 1)) / 16  (mu_q: the mean quantisation    */
+/*         of the token-conditioned mean, as for every coefficient)           */
+/* mu' is exact in fp32 and quantises back to mu_q + k, so the odd rows are   */
+/* an ordinary coefficient stream whose means are mu'.                        */
+/* ------------------------------------------------------------------------ */
+static int64_t floor_shift(int64_t v, uint32_t s) {
+  int64_t d = (int64_t)1 << s;
+  return v >= 0 ? v / d : -((-v + d - 1) / d);
+}
+static int64_t clamp64(int64_t v, int64_t lo, int64_t hi) { return v < lo ? lo : (v > hi ? hi : v); }
+
+int or_ctx_means(uint32_t C, uint32_t R, const int8_t *V, const int8_t *U, uint32_t s1, uint32_t s2,
+                 const int16_t *q_even, uint64_t n_even, const float *mu_odd, uint64_t n_odd, float *out) {
+  if (C == 0 || R == 0 || s1 > 30 || s2 > 30 || n_odd > n_even) return OR_ERR_ARG;
+  int64_t *x = (int64_t *)malloc(C * sizeof(int64_t));
+  int64_t *g = (int64_t *)malloc(R * sizeof(int64_t));
+  if (!x || !g) { free(x); free(g); return OR_ERR_ARG; }
+  for (uint64_t t = 0; t < n_odd; t++) {
+    for (uint32_t c = 0; c < C; c++) {
+      int64_t a = q_even[t * C + c], b = t + 1 < n_even ? q_even[(t + 1) * C + c] : 0;
+      x[c] = clamp64(a + b, -127, 127);
+    }
+    for (uint32_t r = 0; r < R; r++) {
+      int64_t h = 0;
+      for (uint32_t c = 0; c < C; c++) h += (int64_t)V[(uint64_t)r * C + c] * x[c];
+      g[r] = clamp64(floor_shift(h, s1), -127, 127);
+    }
+    for (uint32_t c = 0; c < C; c++) {
+      int64_t y = 0;
+      for (uint32_t r = 0; r < R; r++) y += (int64_t)U[(uint64_t)c * R + r] * g[r];
+      int32_t m; uint32_t f;
+      coef_mean(mu_odd[t * C + c], &m, &f);
+      int64_t mq = 16 * (int64_t)m + f;
+      int64_t mq2 = clamp64(mq + floor_shift(y, s2), -8388607, 8388607);
+      out[t * C + c] = (float)mq2 / 16.0f;
+    }
+  }
+  free(x); free(g);
+  return OR_OK;
+}
