@@ -342,6 +342,8 @@ def main_ours(args):
     }
     if args.paged and w.dtype != synth.COEF:
         res["paged"] = paged_run(args, w, codec, tgt, prd, stream, total, peak)
+    if args.checkerboard and w.dtype == synth.COEF:
+        res["checkerboard"] = checkerboard_run(args, w, stream, dev)
     if args.e2e and world >= 1:
         res["e2e"] = e2e(args, w, codec, tgt, prd, cal, out, stream, dev, total)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -457,6 +459,72 @@ def paged_run(args, w, codec, tgt, prd, stream, total, peak):
             "check": "stream, offsets and decoded pool equal the dense call"}
 
 
+def checkerboard_run(args, w, stream, dev):
+    """The coefficient stream split by token parity with the checkerboard context:
+    even rows coded with their means, odd rows with the context-shifted means
+    (skv_ctx_means: two tensor-core products); decode = even rows, context,
+    odd rows.  Reports the context call's tensor throughput and the ratio
+    against coding the odd rows with their token-conditioned means alone."""
+    import torch
+    from lossless_kv_cache_fp8_gb300 import native, synth
+    qe, qo, me, mo, beta, V, U = synth.gen_coef_checkerboard(w, dev)
+    s1, s2 = synth.CTX_SHIFT1, synth.CTX_SHIFT2
+    C, n_e, n_o, R = qe.shape[1], qe.shape[0], qo.shape[0], V.shape[0]
+    cmap = native.ctx_map(V, U, s1, s2)
+    scratch = torch.empty(native.skv_ctx_scratch_bytes(n_o, C, R), dtype=torch.uint8, device=dev)
+    mo2 = torch.empty_like(mo)
+    ce = native.Codec(native.coef_params(n_e, C, w.lane_syms), device=dev)
+    co = native.Codec(native.coef_params(n_o, C, w.lane_syms), device=dev)
+    for c in (ce, co):
+        c.calibrate(None, beta)
+        c.build_tables()
+
+    def ctx(q_even):
+        assert native.skv_ctx_means(cmap, q_even, n_e, mo, n_o, C, mo2, scratch) == native.SKV_OK
+
+    ctx(qe)
+    ne, no = ce.encode(qe, me), co.encode(qo, mo2)
+    co_plain = native.Codec(native.coef_params(n_o, C, w.lane_syms), device=dev)
+    co_plain.calibrate(None, beta)
+    co_plain.build_tables()
+    n_plain = co_plain.encode(qo, mo)
+    del co_plain
+    qe_d, qo_d = torch.empty_like(qe), torch.empty_like(qo)
+
+    def enc():
+        ce.encode(qe, me, want_total=False)
+        ctx(qe)
+        co.encode(qo, mo2, want_total=False)
+
+    def dec():
+        ce.decode(me, qe_d)
+        ctx(qe_d)
+        co.decode(mo2, qo_d)
+
+    ms = {}
+    for name, fn in (("context", lambda: ctx(qe)), ("encode", enc), ("decode", dec)):
+        for _ in range(args.warmup):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms[name] = e0.elapsed_time(e1) / args.steps
+    assert ce.check() == native.SKV_OK and co.check() == native.SKV_OK
+    assert torch.equal(qe_d, qe) and torch.equal(qo_d, qo)
+    raw = (n_e + n_o) * C * 2
+    flops = 2.0 * n_o * C * R * 2
+    pk = peaks() or {}
+    tpeak = float(pk.get("bf16_tflops") or 1900.0)
+    tf = flops / ms["context"] / 1e9
+    return {"rows": [n_e, n_o], "rank": R, "context_ms": ms["context"], "encode_ms": ms["encode"],
+            "decode_ms": ms["decode"], "context_tflops": tf, "context_tensor_frac": tf / tpeak,
+            "ratio": raw / (ne + no), "odd_rows_bytes": no, "odd_rows_bytes_without_context": n_plain,
+            "check": "both parities decode to the input; context bit-exact with the oracle in tests"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -468,6 +536,8 @@ def main():
     ap.add_argument("--cap-frac", type=float, default=0.6, help="bitstream buffer / raw bytes")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--paged", type=int, default=0, help="also time paged pools with this many tokens per block")
+    ap.add_argument("--checkerboard", action="store_true",
+                    help="coefficient workloads: also time the checkerboard context (two-pass) coding")
     ap.add_argument("--model", type=int, default=0, choices=[0, 1],
                     help="residual model: 0 per-channel scale (default), 1 exponent-normalised (FP8)")
     ap.add_argument("--e2e-steps", type=int, default=3)

@@ -244,6 +244,39 @@ int skv_decode_paged(const skv_params* p, const skv_paged_layout* layout, const 
                      const void* d_tables, const uint8_t* d_bins, void* d_target_pool_out, uint32_t* d_status,
                      void* stream);
 
+/* Checkerboard context for coefficient streams ([DCKV] how it differs: the
+ * compressed rows are split by token parity; even rows are coded with the
+ * token-conditioned means alone, odd rows with means that also use the
+ * already decoded rows on both sides through a rank-1024 linear map, so each
+ * parity decodes in one token-parallel pass).  The page's map is learned; this
+ * call takes any integer map of the same shape (the caller's, e.g. a seeded
+ * one) and computes, for odd row t (token 2t + 1),
+ *   x   = clamp(q_even[t] + q_even[t + 1], -127, 127)   (no row t+1: 0)
+ *   g_r = clamp(floor((V x)_r / 2^shift1), -127, 127)
+ *   k_c = floor((U g)_c / 2^shift2)                     (1/16 steps)
+ *   mu' = clamp(mu_q + k, -(2^23 - 1), 2^23 - 1) / 16
+ * with V, U entries used clamped to [-8, 8] and mu_q = floor(16 mu + 1/2) the
+ * coefficient mean quantisation of d_mu_odd (the token-conditioned means of
+ * the odd rows).  mu' is exact in fp32 and quantises back to mu_q + k, so the
+ * odd rows are an ordinary COEF stream (skv_encode / skv_decode with n_tokens
+ * = n_odd and d_pred = mu'), coded after (and decoded after) the even rows'
+ * stream (n_tokens = n_even, d_pred = their means).
+ * Rows are [row][n_coef] (q int16, means fp32); n_odd <= n_even, n_odd below
+ * 8388480.  Both
+ * products run on tensor cores and are exact (small integers, fp32 sums below
+ * 2^24).  n_coef and rank: multiples of 32 up to 16384; shifts <= 30.
+ * d_scratch: skv_ctx_scratch_bytes(n_odd, n_coef, rank) bytes, 16-aligned. */
+typedef struct {
+  const int8_t* d_V;   /* [rank][n_coef] */
+  const int8_t* d_U;   /* [n_coef][rank] */
+  uint32_t rank;
+  uint32_t shift1, shift2;
+} skv_ctx_map;
+uint64_t skv_ctx_scratch_bytes(uint64_t n_odd, uint32_t n_coef, uint32_t rank);
+int skv_ctx_means(const skv_ctx_map* map, const int16_t* d_q_even, uint64_t n_even, const float* d_mu_odd,
+                  uint64_t n_odd, uint32_t n_coef, float* d_mu_out, void* d_scratch, uint64_t scratch_bytes,
+                  void* stream);
+
 /* Encode without a caller-provided workspace.  The pages have no counterpart
  * to this call; it exists for callers that cannot allocate device memory, such
  * as code handed only its input and output buffers by a host framework that

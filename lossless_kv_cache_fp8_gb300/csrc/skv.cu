@@ -31,6 +31,7 @@
 //   k_*_coef          the same for transform-coefficient streams (1024 tables
 //                     read through L1/L2; switched-off components skipped)
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -1394,6 +1395,134 @@ __global__ void __launch_bounds__(256) k_decode_coef(CodecArgs a) {
 }
 
 // ---------------------------------------------------------------------------
+// Checkerboard context ([DCKV] how it differs): the means of the odd token
+// rows of a coefficient stream from the decoded even rows on both sides,
+// through a rank-R linear map with int8 factors V [R][C], U [C][R]:
+//   x = clamp(q_even[t] + q_even[t + 1], +-127)
+//   g = clamp(floor(V x / 2^s1), +-127),   k = floor(U g / 2^s2)
+//   mu' = clamp(mu_q + k, +-(2^23 - 1)) / 16   (mu_q: the mean quantisation)
+// The map's entries are used clamped to [-8, 8] (4-bit weights kept in int8).
+// Both products run on the tensor cores in bf16 with fp32 accumulation and
+// are exact: operands are small integers (|x|, |g| <= 127, |w| <= 8) and
+// every partial sum stays below K * 127 * 8 < 2^24 for K <= 16384 (checked on
+// the host), so any summation order gives the same integer.
+// ---------------------------------------------------------------------------
+constexpr int kGemmBM = 128, kGemmBN = 128, kGemmBK = 32;
+constexpr int kGemmLd = kGemmBK + 8;    // smem row pitch (bf16): 80 bytes, conflict-free fragment reads
+
+__global__ void __launch_bounds__(256) k_ctx_x(const int16_t* qe, uint64_t n_even, uint64_t n_odd, uint32_t C,
+                                              __nv_bfloat16* X) {
+  const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_odd * C) return;
+  const uint64_t t = i / C, c = i - t * C;
+  int v = qe[t * C + c] + (t + 1 < n_even ? qe[(t + 1) * C + c] : 0);
+  v = v < -127 ? -127 : (v > 127 ? 127 : v);
+  X[i] = __int2bfloat16_rn(v);
+}
+
+// bf16 m16n8k16 tensor-core product, fp32 accumulators
+__device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, const uint32_t* b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// Out[M][N] = epilogue(A[M][K] . B[N][K]^T): A bf16 row-major, B int8 row-major
+// (converted to bf16 while staging).  128 x 128 tiles, 8 warps of 64 x 32.
+// EPI 0: G = bf16(clamp(floor(acc / 2^s), +-127));  EPI 1: mu' from mu and
+// floor(acc / 2^s).  K is a multiple of 32 (checked on the host).
+template <int EPI>
+__global__ void __launch_bounds__(256) k_ctx_gemm(const __nv_bfloat16* A, const int8_t* B, uint32_t M, uint32_t N,
+                                                  uint32_t K, uint32_t s, __nv_bfloat16* G, const float* mu,
+                                                  float* out) {
+  __shared__ __align__(16) __nv_bfloat16 sa[kGemmBM * kGemmLd];
+  __shared__ __align__(16) __nv_bfloat16 sb[kGemmBN * kGemmLd];
+  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t m0 = blockIdx.y * kGemmBM, n0 = blockIdx.x * kGemmBN;
+  const uint32_t wm = (warp >> 2) * 64, wn = (warp & 3) * 32;
+  float acc[4][4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) acc[i][j][r] = 0.f;
+  for (uint32_t k0 = 0; k0 < K; k0 += kGemmBK) {
+    // stage A: 128 rows x 32 bf16 (64 B) -> two 16-byte pieces per thread
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const uint32_t idx = tid + u * 256, row = idx >> 2, part = idx & 3;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (m0 + row < M) v = *reinterpret_cast<const uint4*>(A + (uint64_t)(m0 + row) * K + k0 + part * 8);
+      *reinterpret_cast<uint4*>(sa + row * kGemmLd + part * 8) = v;
+    }
+    // stage B: 128 rows x 32 int8 (32 B) -> one 16-byte piece per thread, to bf16
+    {
+      const uint32_t row = tid >> 1, part = tid & 1;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (n0 + row < N) v = *reinterpret_cast<const uint4*>(B + (uint64_t)(n0 + row) * K + k0 + part * 16);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      __nv_bfloat16* dst = sb + row * kGemmLd + part * 16;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        int wv = (int)(int8_t)(w[q >> 2] >> (8 * (q & 3)));
+        wv = wv < -8 ? -8 : (wv > 8 ? 8 : wv);
+        dst[q] = __int2bfloat16_rn(wv);
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < kGemmBK; kk += 16) {
+      uint32_t af[4][4], bf[4][2];
+      const uint32_t ar = lane >> 2, ac = kk + (lane & 3) * 2;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat16* base = sa + (wm + i * 16 + ar) * kGemmLd + ac;
+        af[i][0] = *reinterpret_cast<const uint32_t*>(base);
+        af[i][1] = *reinterpret_cast<const uint32_t*>(base + 8 * kGemmLd);
+        af[i][2] = *reinterpret_cast<const uint32_t*>(base + 8);
+        af[i][3] = *reinterpret_cast<const uint32_t*>(base + 8 * kGemmLd + 8);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const __nv_bfloat16* base = sb + (wn + j * 8 + ar) * kGemmLd + ac;
+        bf[j][0] = *reinterpret_cast<const uint32_t*>(base);
+        bf[j][1] = *reinterpret_cast<const uint32_t*>(base + 8);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mma_bf16(acc[i][j], af[i], bf[j]);
+    }
+    __syncthreads();
+  }
+  // epilogue: accumulator (row lane/4 [+8], cols 2 (lane%4) [+1]) of each 16 x 8 tile
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const uint32_t m = m0 + wm + i * 16 + (lane >> 2) + (r >> 1) * 8;
+        const uint32_t n = n0 + wn + j * 8 + (lane & 3) * 2 + (r & 1);
+        if (m >= M || n >= N) continue;
+        const int v = (int)acc[i][j][r] >> s;        // the accumulator is an exact integer
+        if (EPI == 0) {
+          G[(uint64_t)m * N + n] = __int2bfloat16_rn(v < -127 ? -127 : (v > 127 ? 127 : v));
+        } else {
+          int mm;
+          uint32_t ff;
+          coef_mean(mu[(uint64_t)m * N + n], &mm, &ff);
+          long long q = 16ll * mm + ff + v;
+          q = q < -8388607 ? -8388607 : (q > 8388607 ? 8388607 : q);
+          out[(uint64_t)m * N + n] = (float)q / 16.0f;
+        }
+      }
+}
+
+// ---------------------------------------------------------------------------
 // Lane lengths -> byte offsets: three-phase exclusive scan, then compaction.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_scan_reduce(const uint32_t* lw, uint64_t n,
@@ -1862,6 +1991,36 @@ int skv_decode_paged(const skv_params* p, const skv_paged_layout* layout, const 
   if (st != SKV_OK) return st;
   return decode_impl(p, &pg, d_bitstream, n_bytes, d_lane_offsets, d_pred_pool, d_tables, d_bins,
                      d_target_pool_out, d_status, stream);
+}
+
+uint64_t skv_ctx_scratch_bytes(uint64_t n_odd, uint32_t n_coef, uint32_t rank) {
+  return align256(n_odd * n_coef * 2) + align256(n_odd * rank * 2);
+}
+
+int skv_ctx_means(const skv_ctx_map* map, const int16_t* d_q_even, uint64_t n_even, const float* d_mu_odd,
+                  uint64_t n_odd, uint32_t n_coef, float* d_mu_out, void* d_scratch, uint64_t scratch_bytes,
+                  void* stream) {
+  if (!map || !map->d_V || !map->d_U) return SKV_ERR_INVALID_ARG;
+  const uint32_t R = map->rank, C = n_coef;
+  if (R == 0 || R % 32 || R > 16384 || C == 0 || C % 32 || C > 16384 || map->shift1 > 30 || map->shift2 > 30)
+    return SKV_ERR_INVALID_ARG;
+  if (n_odd > n_even || n_odd > 65535ull * kGemmBM) return SKV_ERR_INVALID_ARG;   // grid rows
+  if (n_odd == 0) return SKV_OK;
+  if (!d_q_even || !d_mu_odd || !d_mu_out || !d_scratch || !aligned16(d_q_even) || !aligned16(d_mu_odd) ||
+      !aligned16(d_mu_out) || !aligned16(d_scratch) || !aligned16(map->d_V) || !aligned16(map->d_U))
+    return SKV_ERR_INVALID_ARG;
+  if (scratch_bytes < skv_ctx_scratch_bytes(n_odd, C, R)) return SKV_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  __nv_bfloat16* X = static_cast<__nv_bfloat16*>(d_scratch);
+  __nv_bfloat16* G = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(d_scratch) + align256(n_odd * C * 2));
+  const uint64_t nx = n_odd * C;
+  k_ctx_x<<<(unsigned)((nx + 255) / 256), 256, 0, s>>>(d_q_even, n_even, n_odd, C, X);
+  const unsigned gm = (unsigned)((n_odd + kGemmBM - 1) / kGemmBM);
+  k_ctx_gemm<0><<<dim3((R + kGemmBN - 1) / kGemmBN, gm), 256, 0, s>>>(X, map->d_V, (uint32_t)n_odd, R, C,
+                                                                        map->shift1, G, nullptr, nullptr);
+  k_ctx_gemm<1><<<dim3((C + kGemmBN - 1) / kGemmBN, gm), 256, 0, s>>>(G, map->d_U, (uint32_t)n_odd, C, R,
+                                                                        map->shift2, nullptr, d_mu_odd, d_mu_out);
+  return launch_check();
 }
 
 // Scratch of skv_encode_noalloc: a file-scope device array, so the call never

@@ -41,6 +41,16 @@ class skv_paged_layout(C.Structure):
     _fields_ = [("d_block_table", C.c_void_p), ("n_blocks", C.c_uint32), ("block_tokens", C.c_uint32)]
 
 
+class skv_ctx_map(C.Structure):
+    _fields_ = [("d_V", C.c_void_p), ("d_U", C.c_void_p), ("rank", C.c_uint32), ("shift1", C.c_uint32),
+                ("shift2", C.c_uint32)]
+
+
+def ctx_map(V, U, shift1: int, shift2: int) -> skv_ctx_map:
+    """map of int8 device tensors V [rank][n_coef], U [n_coef][rank]"""
+    return skv_ctx_map(_ptr(V), _ptr(U), V.shape[0], shift1, shift2)
+
+
 def paged_layout(block_table, n_blocks: int, block_tokens: int) -> skv_paged_layout:
     """layout of paged pools; block_table: a uint32-valued device tensor (int32 storage)"""
     return skv_paged_layout(_ptr(block_table), n_blocks, block_tokens)
@@ -67,6 +77,7 @@ def params_for(w, model: int = 0) -> skv_params:
 _lib = None
 _P = C.POINTER(skv_params)
 _PL = C.POINTER(skv_paged_layout)
+_CM = C.POINTER(skv_ctx_map)
 _SIGS = {
     "skv_status_string": (C.c_char_p, [C.c_int]),
     "skv_check_params": (C.c_int, [_P]),
@@ -96,6 +107,9 @@ _SIGS = {
                                    C.c_void_p]),
     "skv_decode_paged": (C.c_int, [_P, _PL, C.c_void_p, C.c_uint64, C.c_void_p, C.c_void_p, C.c_void_p,
                                    C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
+    "skv_ctx_scratch_bytes": (C.c_uint64, [C.c_uint64, C.c_uint32, C.c_uint32]),
+    "skv_ctx_means": (C.c_int, [_CM, C.c_void_p, C.c_uint64, C.c_void_p, C.c_uint64, C.c_uint32, C.c_void_p,
+                                C.c_void_p, C.c_uint64, C.c_void_p]),
 }
 
 
@@ -206,6 +220,18 @@ def skv_selftest_lookback(state, n_chunks, missing_chunk, max_spins, excl, statu
 
 def skv_read_status(status, stream=None) -> int:
     return lib().skv_read_status(_ptr(status), _stream(stream))
+
+
+# --- checkerboard context (same names as the C ABI) ----------------------------------------------
+def skv_ctx_scratch_bytes(n_odd: int, n_coef: int, rank: int) -> int:
+    return lib().skv_ctx_scratch_bytes(n_odd, n_coef, rank)
+
+
+def skv_ctx_means(cmap, q_even, n_even, mu_odd, n_odd, n_coef, mu_out, scratch, scratch_bytes=None,
+                  stream=None) -> int:
+    nb = scratch_bytes if scratch_bytes is not None else scratch.numel() * scratch.element_size()
+    return lib().skv_ctx_means(C.byref(cmap), _ptr(q_even), n_even, _ptr(mu_odd), n_odd, n_coef, _ptr(mu_out),
+                               _ptr(scratch), nb, _stream(stream))
 
 
 # --- paged pools (same names as the C ABI) -----------------------------------------------------

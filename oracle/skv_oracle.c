@@ -778,7 +778,8 @@ int or_symbols(const or_params *p, const uint8_t *bins, const void *target, cons
 /* means alone, odd rows with means that also depend on the decoded rows on   */
 /* both sides through a rank-R linear map, so each parity decodes in one      */
 /* token-parallel pass.  READING (the page's map is learned; none is given):  */
-/* an integer map with factor matrices V [R][C], U [C][R] (int8), and         */
+/* an integer map with factor matrices V [R][C], U [C][R] (int8 storage,      */
+/* entries used clamped to [-8, 8]: 4-bit weights), and                       */
 /*   x   = clamp(q_even[t] + q_even[t+1], -127, 127)  (missing row -> 0)      */
 /*   g_r = clamp(floor((V x)_r / 2^s1), -127, 127)                            */
 /*   k_c = floor((U g)_c / 2^s2)               (context shift, 1/16 steps)    */
@@ -806,12 +807,12 @@ int or_ctx_means(uint32_t C, uint32_t R, const int8_t *V, const int8_t *U, uint3
     }
     for (uint32_t r = 0; r < R; r++) {
       int64_t h = 0;
-      for (uint32_t c = 0; c < C; c++) h += (int64_t)V[(uint64_t)r * C + c] * x[c];
+      for (uint32_t c = 0; c < C; c++) h += clamp64(V[(uint64_t)r * C + c], -8, 8) * x[c];
       g[r] = clamp64(floor_shift(h, s1), -127, 127);
     }
     for (uint32_t c = 0; c < C; c++) {
       int64_t y = 0;
-      for (uint32_t r = 0; r < R; r++) y += (int64_t)U[(uint64_t)c * R + r] * g[r];
+      for (uint32_t r = 0; r < R; r++) y += clamp64(U[(uint64_t)c * R + r], -8, 8) * g[r];
       int32_t m; uint32_t f;
       coef_mean(mu_odd[t * C + c], &m, &f);
       int64_t mq = 16 * (int64_t)m + f;

@@ -11,7 +11,7 @@ from lossless_kv_cache_fp8_gb300 import synth
 
 
 def _numpy_ctx(V, U, s1, s2, qe, mo):
-    V = V.astype(np.int64); U = U.astype(np.int64)
+    V = np.clip(V.astype(np.int64), -8, 8); U = np.clip(U.astype(np.int64), -8, 8)
     n_o = mo.shape[0]
     right = np.zeros((n_o, qe.shape[1]), np.int64)
     n_r = min(n_o, qe.shape[0] - 1)
@@ -29,6 +29,8 @@ def test_ctx_means_match_definition(orc):
     for (C, R, n_e, n_o) in [(48, 16, 7, 7), (40, 24, 9, 8), (16, 8, 1, 1)]:
         V = rng.integers(-8, 9, (R, C)).astype(np.int8)
         U = rng.integers(-8, 9, (C, R)).astype(np.int8)
+        V[0, :3] = [127, -128, 9]          # entries outside [-8, 8] are used clamped
+        U[1, :2] = [-100, 50]
         qe = rng.integers(-200, 201, (n_e, C)).astype(np.int16)
         qe[0, :5] = [32767, -32768, 127, -128, 0]
         mo = (rng.standard_normal((n_o, C)) * 50).astype(np.float32)
