@@ -842,7 +842,7 @@ __device__ unsigned long long chunk_lookback(unsigned long long* st, uint64_t c,
 
 // Warp-cooperative copy of n_w 16-bit words from src to dst (both 2-byte
 // aligned): 32-bit accesses, a 16-bit funnel when the two differ by 2 mod 4,
-// four independent loads in flight per thread.
+// sixteen independent loads in flight per thread (the copy is latency bound).
 __device__ __forceinline__ void warp_copy_words(uint16_t* dst, const uint16_t* src, uint32_t n_w, uint32_t tid) {
   if (n_w == 0) return;
   if ((reinterpret_cast<uintptr_t>(dst) & 3) != 0) {   // make dst 4-byte aligned
@@ -853,31 +853,31 @@ __device__ __forceinline__ void warp_copy_words(uint16_t* dst, const uint16_t* s
   uint32_t* d32 = reinterpret_cast<uint32_t*>(dst);
   if ((reinterpret_cast<uintptr_t>(src) & 3) == 0) {
     const uint32_t* s32 = reinterpret_cast<const uint32_t*>(src);
-    for (uint32_t k0 = 0; k0 < n32; k0 += 128) {
-      uint32_t v[4];
+    for (uint32_t k0 = 0; k0 < n32; k0 += 512) {
+      uint32_t v[16];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 16; ++u) {
         const uint32_t k = k0 + u * 32 + tid;
         v[u] = k < n32 ? __ldcs(s32 + k) : 0u;
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 16; ++u) {
         const uint32_t k = k0 + u * 32 + tid;
         if (k < n32) d32[k] = v[u];
       }
     }
   } else {
     const uint32_t* s32 = reinterpret_cast<const uint32_t*>(src - 1);   // aligned, one word early
-    for (uint32_t k0 = 0; k0 < n32; k0 += 128) {
-      uint32_t lo[4], hi[4];
+    for (uint32_t k0 = 0; k0 < n32; k0 += 512) {
+      uint32_t lo[16], hi[16];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 16; ++u) {
         const uint32_t k = k0 + u * 32 + tid;
         lo[u] = k < n32 ? __ldcs(s32 + k) : 0u;
         hi[u] = k < n32 ? __ldcs(s32 + k + 1) : 0u;
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 16; ++u) {
         const uint32_t k = k0 + u * 32 + tid;
         if (k < n32) d32[k] = __funnelshift_r(lo[u], hi[u], 16);
       }
