@@ -344,10 +344,12 @@ __device__ __forceinline__ void dec_close(const DecLane& L, uint32_t* status) {
 }
 
 // Decoder lane reading its words through a 64-byte shared-memory ring of
-// aligned 16-byte stream blocks (block k lives in ring slot k mod 4).  The
-// block after the ring is staged in registers one refill ahead.  Offsets are
-// relative to base = the lane's first byte rounded down to 64, so the ring
-// index of byte offset p is p & 63.
+// aligned 16-byte stream blocks (block k lives in ring slot k mod 4), filled
+// by asynchronous copies: a refill first waits for the copies issued at the
+// previous refill, then issues the blocks that keep [p/16, p/16 + 4) resident.
+// A lane consumes at most 32 stream bytes between refills, so it never reads
+// the block issued at the latest refill before the next one.  Offsets are
+// relative to base = the lane's first byte rounded down to 64.
 struct RingLane {
   const uint8_t* base; // bitstream + (lane start & ~63)
   uint32_t ring;       // shared-window address of the ring (64-byte aligned)
@@ -355,25 +357,34 @@ struct RingLane {
   uint32_t end;        // one past the lane's last byte
   uint32_t rb;         // next block to move into the ring
   uint32_t last;       // last block holding lane bytes (rb > last: nothing left)
-  uint4 stage;         // block rb, loaded ahead
   uint32_t nxt, x;
 };
 __device__ __forceinline__ uint4 load_block(const RingLane& L, uint32_t k) {
   return k <= L.last ? ldg_stream(L.base + ((uint64_t)k << 4)) : make_uint4(0, 0, 0, 0);
 }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// block rb -> ring slot rb mod 4 (zero bytes read past the lane's last block)
+__device__ __forceinline__ void ring_step(RingLane& L) {
+  const uint32_t saddr = (uint32_t)__cvta_generic_to_shared(g_smem + L.ring + (L.rb & 3u) * 16u);
+  const bool valid = L.rb <= L.last;
+  const uint8_t* src = L.base + (valid ? ((uint64_t)L.rb << 4) : 0);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr), "l"(src), "r"(valid ? 16u : 0u)
+               : "memory");
+  ++L.rb;
+}
 // make blocks [p/16, p/16 + 4) resident: one straight-line step covers a lane
 // that moved into a new block since the last refill; lanes that moved further
-// (escape-heavy stretches) catch up in a warp-uniform loop
-__device__ __forceinline__ void ring_step(RingLane& L) {
-  sts_u128(L.ring + (L.rb & 3u) * 16u, L.stage);
-  ++L.rb;
-  L.stage = load_block(L, L.rb);
-}
+// (escape-heavy stretches) catch up in a warp-uniform loop and wait for their
+// copies at once
 __device__ __forceinline__ void ring_refill(RingLane& L, uint32_t act) {
-  if (L.rb < (L.p >> 4) + 4) ring_step(L);
+  cp_async_wait_all();
+  uint32_t n = 0;
+  if (L.rb < (L.p >> 4) + 4) { ring_step(L); ++n; }
   while (__any_sync(act, L.rb < (L.p >> 4) + 4)) {
-    if (L.rb < (L.p >> 4) + 4) ring_step(L);
+    if (L.rb < (L.p >> 4) + 4) { ring_step(L); ++n; }
   }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  if (n > 1) cp_async_wait_all();
 }
 __device__ __forceinline__ uint32_t ring_word(const RingLane& L, uint32_t p) {
   return lds_u16((p & (kRingBytes - 1)) + L.ring);
@@ -401,7 +412,6 @@ __device__ __forceinline__ uint32_t ring_raw_if(RingLane& L, bool do_it) {
 __device__ __forceinline__ void ring_open(RingLane& L, const uint8_t* bs, uint32_t ring, uint64_t a, uint64_t b,
                                           bool ok, uint32_t* status) {
   L.ring = ring;
-  L.stage = make_uint4(0, 0, 0, 0);
   if (!ok) {   // nothing is read from global memory for a lane with bad offsets
     if (status) atomicOr(status, SKV_FLAG_CORRUPT);   // NULL: an idle lane, not an error
     L.base = bs;
@@ -419,21 +429,19 @@ __device__ __forceinline__ void ring_open(RingLane& L, const uint8_t* bs, uint32
   for (uint32_t k = first; k < first + 4; ++k)
     if (k <= L.last) sts_u128(ring + (k & 3u) * 16u, ldg_stream(L.base + ((uint64_t)k << 4)));
   L.rb = first + 4;
-  L.stage = load_block(L, L.rb);
   L.x = (ring_word(L, L.p) << 16) | ring_word(L, L.p + 2);
   L.p += 4;
   L.nxt = ring_word(L, L.p);
   if (L.x < kStateLow && status) atomicOr(status, SKV_FLAG_CORRUPT);
 }
 // Reposition the ring at stream offset p (relative to base, at or after the
-// lane's first byte): reload the four blocks from p's block on and the staged
-// block after them.
+// lane's first byte): reload the four blocks from p's block on.
 __device__ __forceinline__ void ring_reopen(RingLane& L, uint32_t p) {
+  cp_async_wait_all();   // no earlier copy may still land in the ring
   const uint32_t first = p >> 4;
   for (uint32_t k = first; k < first + 4; ++k) sts_u128(L.ring + (k & 3u) * 16u, load_block(L, k));
   L.p = p;
   L.rb = first + 4;
-  L.stage = load_block(L, L.rb);
 }
 __device__ __forceinline__ void ring_close(const RingLane& L, uint32_t* status) {
   if (L.x != kStateLow || L.p != L.end) atomicOr(status, SKV_FLAG_CORRUPT);
