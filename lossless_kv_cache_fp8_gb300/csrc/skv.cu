@@ -62,9 +62,12 @@ constexpr uint32_t kRingBytes = 64;                                // per-lane s
 #endif
 constexpr uint32_t kRingStride = SKV_RING_STRIDE;   // spacing of the lanes' rings (16-byte multiple)
 #ifndef SKV_CODEC_THREADS
-#define SKV_CODEC_THREADS 768
+#define SKV_CODEC_THREADS 1024
 #endif
 constexpr int kCodecThreads = SKV_CODEC_THREADS;   // decoder threads per CTA (one CTA per SM)
+// the paged and exponent-model decoders keep more state per lane: 768 threads
+// leave them enough registers not to spill
+constexpr int dec_threads(bool paged, bool model) { return (paged || model) && kCodecThreads > 768 ? 768 : kCodecThreads; }
 #ifndef SKV_ENC_THREADS
 #define SKV_ENC_THREADS 768
 #endif
@@ -1161,7 +1164,7 @@ __device__ __forceinline__ void dec_exact(RingLane& L, uint32_t tbe, uint32_t pw
 }
 
 template <int ESZ, bool PAGED, bool MODEL>
-__global__ void __launch_bounds__(kCodecThreads, 1) k_decode_kv(CodecArgs a) {
+__global__ void __launch_bounds__(dec_threads(PAGED, MODEL), 1) k_decode_kv(CodecArgs a) {
   constexpr int G = 16 / ESZ;
   constexpr int SUB = ESZ == 1 ? 8 : 4;   // at most 32 / 24 stream bytes between refills
   constexpr uint32_t kBias = ESZ == 1 ? 0x7F7F7F7Fu : 0x007F007Fu;
@@ -1920,9 +1923,10 @@ static int decode_impl(const skv_params* p, const Paged* pg, const void* d_bitst
     return launch_check();
   }
   int blocks, threads;
-  codec_grid(g.n_chunks, &blocks, &threads, kCodecThreads);
+  const int max_threads = dec_threads(pg != nullptr, g.model != 0);
+  codec_grid(g.n_chunks, &blocks, &threads, max_threads);
   const int smem_bytes = (int)(kDecTabBytes + (uint32_t)threads * kRingStride);
-  const uint32_t smax = kDecTabBytes + kCodecThreads * kRingStride;
+  const uint32_t smax = kDecTabBytes + max_threads * kRingStride;
   if (pg) a.pg = *pg;
   auto run = [&](auto kern) -> int {
     int e = set_smem(kern, smax);
