@@ -462,7 +462,7 @@ def paged_run(args, w, codec, tgt, prd, stream, total, peak):
 def checkerboard_run(args, w, stream, dev):
     """The coefficient stream split by token parity with the checkerboard context:
     even rows coded with their means, odd rows with the context-shifted means
-    (skv_ctx_means: two tensor-core products); decode = even rows, context,
+    (skv_ctx_means: two tcgen05 tensor-core products); decode = even rows, context,
     odd rows.  Reports the context call's tensor throughput and the ratio
     against coding the odd rows with their token-conditioned means alone."""
     import torch
@@ -479,8 +479,10 @@ def checkerboard_run(args, w, stream, dev):
         c.calibrate(None, beta)
         c.build_tables()
 
+    ctx_status = torch.zeros(4, dtype=torch.int32, device=dev)
+
     def ctx(q_even):
-        assert native.skv_ctx_means(cmap, q_even, n_e, mo, n_o, C, mo2, scratch) == native.SKV_OK
+        assert native.skv_ctx_means(cmap, q_even, n_e, mo, n_o, C, mo2, scratch, ctx_status) == native.SKV_OK
 
     ctx(qe)
     ne, no = ce.encode(qe, me), co.encode(qo, mo2)
@@ -513,6 +515,7 @@ def checkerboard_run(args, w, stream, dev):
         torch.cuda.synchronize()
         ms[name] = e0.elapsed_time(e1) / args.steps
     assert ce.check() == native.SKV_OK and co.check() == native.SKV_OK
+    assert native.skv_read_status(ctx_status) == native.SKV_OK
     assert torch.equal(qe_d, qe) and torch.equal(qo_d, qo)
     raw = (n_e + n_o) * C * 2
     flops = 2.0 * n_o * C * R * 2

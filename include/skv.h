@@ -262,10 +262,17 @@ int skv_decode_paged(const skv_params* p, const skv_paged_layout* layout, const 
  * = n_odd and d_pred = mu'), coded after (and decoded after) the even rows'
  * stream (n_tokens = n_even, d_pred = their means).
  * Rows are [row][n_coef] (q int16, means fp32); n_odd <= n_even, n_odd below
- * 8388480.  Both
- * products run on tensor cores and are exact (small integers, fp32 sums below
- * 2^24).  n_coef and rank: multiples of 32 up to 16384; shifts <= 30.
- * d_scratch: skv_ctx_scratch_bytes(n_odd, n_coef, rank) bytes, 16-aligned. */
+ * 8388480.  Both products run on the 5th-generation tensor cores (tcgen05,
+ * bf16 operands, fp32 accumulators in tensor memory) and are exact (small
+ * integers, fp32 sums below 2^24).  n_coef and rank: multiples of 32 up to
+ * 16384; shifts <= 30.
+ * d_scratch: skv_ctx_scratch_bytes(n_odd, n_coef, rank) bytes, 16-aligned
+ * (x and g as bf16 matrices and bf16 copies of V and U).
+ * d_status: one caller-owned device word, cleared by the call; a kernel that
+ * waited over about a second on its own pipeline sets SKV_FLAG_TIMEOUT
+ * (read it with skv_read_status).  Argument errors return
+ * SKV_ERR_INVALID_ARG and launch nothing; SKV_ERR_UNSUPPORTED if the driver
+ * offers no tensor-map encoder. */
 typedef struct {
   const int8_t* d_V;   /* [rank][n_coef] */
   const int8_t* d_U;   /* [n_coef][rank] */
@@ -275,7 +282,7 @@ typedef struct {
 uint64_t skv_ctx_scratch_bytes(uint64_t n_odd, uint32_t n_coef, uint32_t rank);
 int skv_ctx_means(const skv_ctx_map* map, const int16_t* d_q_even, uint64_t n_even, const float* d_mu_odd,
                   uint64_t n_odd, uint32_t n_coef, float* d_mu_out, void* d_scratch, uint64_t scratch_bytes,
-                  void* stream);
+                  uint32_t* d_status, void* stream);
 
 /* Encode without a caller-provided workspace.  The pages have no counterpart
  * to this call; it exists for callers that cannot allocate device memory, such

@@ -31,6 +31,8 @@
 //   k_*_coef          the same for transform-coefficient streams (1024 tables
 //                     read through L1/L2; switched-off components skipped)
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -1418,8 +1420,83 @@ __global__ void __launch_bounds__(256) k_decode_coef(CodecArgs a) {
 // every partial sum stays below K * 127 * 8 < 2^24 for K <= 16384 (checked on
 // the host), so any summation order gives the same integer.
 // ---------------------------------------------------------------------------
-constexpr int kGemmBM = 128, kGemmBN = 128, kGemmBK = 32;
-constexpr int kGemmLd = kGemmBK + 8;    // smem row pitch (bf16): 80 bytes, conflict-free fragment reads
+constexpr uint32_t kUmBM = 128, kUmBN = 128, kUmBK = 64;   // output tile and k-block (64 bf16 = 128 B rows)
+constexpr uint32_t kUmStages = 4;                            // k-blocks in flight
+constexpr uint32_t kUmTile = kUmBM * kUmBK * 2;              // one operand tile: 16 KB
+constexpr uint32_t kUmSmem = kUmStages * 2 * kUmTile + 1024 + 256;
+// instruction descriptor (kind::f16): fp32 accumulator (bits 4-5 = 1), bf16 A
+// and B (bits 7-9, 10-12 = 1), both K-major, N / 8 at bit 17, M / 16 at bit 24
+constexpr uint32_t kUmIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((kUmBN >> 3) << 17) | ((kUmBM >> 4) << 24);
+constexpr uint64_t kUmWaitNs = 1000000000ull;                // ~1 s bound on every barrier wait
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// wait for the phase of parity `parity` to complete; false after ~1 s
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try(bar, parity))
+    if (global_ns() - t0 > kUmWaitNs) return false;
+  return true;
+}
+// 2-D tile load (x = inner element index, y = row) completing on `bar`
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, uint32_t x, uint32_t y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(tm), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+// shared-memory matrix descriptor: K-major rows of 128 B in the 128-byte
+// swizzle (the layout the tile loads write), 8-row groups 1024 B apart
+__device__ __forceinline__ uint64_t umma_desc(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
+         (2ull << 61);
+}
+__device__ __forceinline__ void umma_bf16(uint32_t tmem, uint64_t da, uint64_t db, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+          tmem),
+      "l"(da), "l"(db), "r"(kUmIdesc), "r"(accumulate));
+}
+// arrive on `bar` once every earlier tcgen05.mma of this thread has completed
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// 32 consecutive fp32 columns of the warp's 32 accumulator rows (one row per thread)
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
 
 __global__ void __launch_bounds__(256) k_ctx_x(const int16_t* qe, uint64_t n_even, uint64_t n_odd, uint32_t C,
                                               __nv_bfloat16* X) {
@@ -1430,107 +1507,133 @@ __global__ void __launch_bounds__(256) k_ctx_x(const int16_t* qe, uint64_t n_eve
   v = v < -127 ? -127 : (v > 127 ? 127 : v);
   X[i] = __int2bfloat16_rn(v);
 }
-
-// bf16 m16n8k16 tensor-core product, fp32 accumulators
-__device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, const uint32_t* b) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+// map factor entries, clamped to [-8, 8], as bf16 operands
+__global__ void __launch_bounds__(256) k_ctx_w(const int8_t* w, uint64_t n, __nv_bfloat16* wb) {
+  const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  int v = w[i];
+  v = v < -8 ? -8 : (v > 8 ? 8 : v);
+  wb[i] = __int2bfloat16_rn(v);
 }
 
-// Out[M][N] = epilogue(A[M][K] . B[N][K]^T): A bf16 row-major, B int8 row-major
-// (converted to bf16 while staging).  128 x 128 tiles, 8 warps of 64 x 32.
+// Out[M][N] = epilogue(A[M][K] . B[N][K]^T), A and B bf16 row-major (K-major),
+// one 128 x 128 output tile per CTA on the 5th-generation tensor cores:
+// thread 0 streams k-blocks of both operands into a 4-deep ring of
+// shared-memory stages with tile loads, thread 32 issues the MMAs into a
+// 128 x 128 fp32 accumulator in tensor memory and releases each stage when its
+// MMAs complete, then all four warps read the accumulator rows back (warp w:
+// rows 32w..32w+31).  Rows past M and k past K load as zeros.
 // EPI 0: G = bf16(clamp(floor(acc / 2^s), +-127));  EPI 1: mu' from mu and
-// floor(acc / 2^s).  K is a multiple of 32 (checked on the host).
+// floor(acc / 2^s).  N is a multiple of 32 (checked on the host).
 template <int EPI>
-__global__ void __launch_bounds__(256) k_ctx_gemm(const __nv_bfloat16* A, const int8_t* B, uint32_t M, uint32_t N,
-                                                  uint32_t K, uint32_t s, __nv_bfloat16* G, const float* mu,
-                                                  float* out) {
-  __shared__ __align__(16) __nv_bfloat16 sa[kGemmBM * kGemmLd];
-  __shared__ __align__(16) __nv_bfloat16 sb[kGemmBN * kGemmLd];
-  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t m0 = blockIdx.y * kGemmBM, n0 = blockIdx.x * kGemmBN;
-  const uint32_t wm = (warp >> 2) * 64, wn = (warp & 3) * 32;
-  float acc[4][4][4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) acc[i][j][r] = 0.f;
-  for (uint32_t k0 = 0; k0 < K; k0 += kGemmBK) {
-    // stage A: 128 rows x 32 bf16 (64 B) -> two 16-byte pieces per thread
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const uint32_t idx = tid + u * 256, row = idx >> 2, part = idx & 3;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (m0 + row < M) v = *reinterpret_cast<const uint4*>(A + (uint64_t)(m0 + row) * K + k0 + part * 8);
-      *reinterpret_cast<uint4*>(sa + row * kGemmLd + part * 8) = v;
+__global__ void __launch_bounds__(128, 1) k_ctx_umma(const __grid_constant__ CUtensorMap tmA,
+                                                     const __grid_constant__ CUtensorMap tmB, uint32_t M, uint32_t N,
+                                                     uint32_t K, uint32_t s, __nv_bfloat16* G, const float* mu,
+                                                     float* out, uint32_t* status) {
+  const uint32_t base = (smem_addr(g_smem) + 1023u) & ~1023u;   // stages need 1024-byte alignment
+  const uint32_t bar_full = base + kUmStages * 2 * kUmTile;
+  const uint32_t bar_empty = bar_full + 8 * kUmStages;
+  const uint32_t bar_done = bar_empty + 8 * kUmStages;
+  const uint32_t tslot = bar_done + 8;
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t m0 = blockIdx.y * kUmBM, n0 = blockIdx.x * kUmBN;
+  const uint32_t nk = (K + kUmBK - 1) / kUmBK;
+  if (threadIdx.x == 0) {
+    for (uint32_t i = 0; i < kUmStages; ++i) {
+      mbar_init(bar_full + 8 * i, 1);
+      mbar_init(bar_empty + 8 * i, 1);
     }
-    // stage B: 128 rows x 32 int8 (32 B) -> one 16-byte piece per thread, to bf16
-    {
-      const uint32_t row = tid >> 1, part = tid & 1;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (n0 + row < N) v = *reinterpret_cast<const uint4*>(B + (uint64_t)(n0 + row) * K + k0 + part * 16);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      __nv_bfloat16* dst = sb + row * kGemmLd + part * 16;
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        int wv = (int)(int8_t)(w[q >> 2] >> (8 * (q & 3)));
-        wv = wv < -8 ? -8 : (wv > 8 ? 8 : wv);
-        dst[q] = __int2bfloat16_rn(wv);
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int kk = 0; kk < kGemmBK; kk += 16) {
-      uint32_t af[4][4], bf[4][2];
-      const uint32_t ar = lane >> 2, ac = kk + (lane & 3) * 2;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat16* base = sa + (wm + i * 16 + ar) * kGemmLd + ac;
-        af[i][0] = *reinterpret_cast<const uint32_t*>(base);
-        af[i][1] = *reinterpret_cast<const uint32_t*>(base + 8 * kGemmLd);
-        af[i][2] = *reinterpret_cast<const uint32_t*>(base + 8);
-        af[i][3] = *reinterpret_cast<const uint32_t*>(base + 8 * kGemmLd + 8);
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const __nv_bfloat16* base = sb + (wn + j * 8 + ar) * kGemmLd + ac;
-        bf[j][0] = *reinterpret_cast<const uint32_t*>(base);
-        bf[j][1] = *reinterpret_cast<const uint32_t*>(base + 8);
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) mma_bf16(acc[i][j], af[i], bf[j]);
-    }
-    __syncthreads();
+    mbar_init(bar_done, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  // epilogue: accumulator (row lane/4 [+8], cols 2 (lane%4) [+1]) of each 16 x 8 tile
+  if (warp == 2) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tslot), "r"(kUmBN));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  uint32_t tmem;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem) : "r"(tslot) : "memory");
+  bool ok = true;
+  if (threadIdx.x == 0) {
+    for (uint32_t kb = 0; kb < nk; ++kb) {
+      const uint32_t st = kb % kUmStages;
+      if (kb >= kUmStages && !mbar_wait(bar_empty + 8 * st, ((kb / kUmStages) - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      const uint32_t dst = base + st * 2 * kUmTile;
+      mbar_expect_tx(bar_full + 8 * st, 2 * kUmTile);
+      tma_load_2d(dst, &tmA, kb * kUmBK, m0, bar_full + 8 * st);
+      tma_load_2d(dst + kUmTile, &tmB, kb * kUmBK, n0, bar_full + 8 * st);
+    }
+  } else if (threadIdx.x == 32) {
+    for (uint32_t kb = 0; kb < nk; ++kb) {
+      const uint32_t st = kb % kUmStages;
+      if (!mbar_wait(bar_full + 8 * st, (kb / kUmStages) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint64_t da = umma_desc(base + st * 2 * kUmTile), db = umma_desc(base + st * 2 * kUmTile + kUmTile);
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+      for (uint32_t k = 0; k < kUmBK / 16; ++k)        // 16 bf16 = 32 bytes along the swizzled row
+        umma_bf16(tmem, da + 2 * k, db + 2 * k, (kb | k) != 0);
+      umma_commit(bar_empty + 8 * st);
+    }
+    umma_commit(bar_done);
+  }
+  __syncwarp();
+  if (!mbar_wait(bar_done, 0)) ok = false;
+  tc_fence_after();
+  const uint32_t row = m0 + warp * 32 + lane;
+#pragma unroll 1
+  for (uint32_t c0 = 0; c0 < kUmBN; c0 += 32) {
+    uint32_t r[32];
+    tmem_ld32(tmem + ((warp * 32u) << 16) + c0, r);
+    const uint32_t n = n0 + c0;
+    if (row >= M || n >= N) continue;
+    const uint64_t o = (uint64_t)row * N + n;
+    if (EPI == 0) {
+      uint32_t h[16];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+      for (int j = 0; j < 16; ++j) {
+        int v0 = (int)__uint_as_float(r[2 * j]) >> s, v1 = (int)__uint_as_float(r[2 * j + 1]) >> s;
+        v0 = v0 < -127 ? -127 : (v0 > 127 ? 127 : v0);
+        v1 = v1 < -127 ? -127 : (v1 > 127 ? 127 : v1);
+        const __nv_bfloat162 b = __halves2bfloat162(__int2bfloat16_rn(v0), __int2bfloat16_rn(v1));
+        h[j] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(G + o);
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const uint32_t m = m0 + wm + i * 16 + (lane >> 2) + (r >> 1) * 8;
-        const uint32_t n = n0 + wn + j * 8 + (lane & 3) * 2 + (r & 1);
-        if (m >= M || n >= N) continue;
-        const int v = (int)acc[i][j][r] >> s;        // the accumulator is an exact integer
-        if (EPI == 0) {
-          G[(uint64_t)m * N + n] = __int2bfloat16_rn(v < -127 ? -127 : (v > 127 ? 127 : v));
-        } else {
+      for (int j = 0; j < 4; ++j) dst[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+    } else {
+      const float4* src = reinterpret_cast<const float4*>(mu + o);
+      float4* dst = reinterpret_cast<float4*>(out + o);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 m4 = src[j];
+        const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+        float res[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
           int mm;
           uint32_t ff;
-          coef_mean(mu[(uint64_t)m * N + n], &mm, &ff);
-          long long q = 16ll * mm + ff + v;
+          coef_mean(mv[u], &mm, &ff);
+          long long q = 16ll * mm + ff + ((int)__uint_as_float(r[4 * j + u]) >> s);
           q = q < -8388607 ? -8388607 : (q > 8388607 ? 8388607 : q);
-          out[(uint64_t)m * N + n] = (float)q / 16.0f;
+          res[u] = (float)q / 16.0f;
         }
+        dst[j] = make_float4(res[0], res[1], res[2], res[3]);
       }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kUmBN));
+  if (!ok) atomicOr(status, SKV_FLAG_TIMEOUT);
 }
 
 // ---------------------------------------------------------------------------
@@ -2006,32 +2109,88 @@ int skv_decode_paged(const skv_params* p, const skv_paged_layout* layout, const 
 }
 
 uint64_t skv_ctx_scratch_bytes(uint64_t n_odd, uint32_t n_coef, uint32_t rank) {
-  return align256(n_odd * n_coef * 2) + align256(n_odd * rank * 2);
+  return align256(n_odd * n_coef * 2) + align256(n_odd * rank * 2) + 2 * align256((uint64_t)rank * n_coef * 2);
 }
+
+}  // extern "C"
+
+namespace {
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link to the driver library)
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (PFN_cuTensorMapEncodeTiled_v12000) nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }();
+  return fn;
+}
+// bf16 matrix [rows][inner] (row pitch inner * 2 bytes) read in 128-row x 64-column
+// boxes in the 128-byte swizzle; out-of-range elements read as zero
+int make_tmap(CUtensorMap* tm, const void* ptr, uint64_t inner, uint64_t rows) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
+  if (!enc) return SKV_ERR_UNSUPPORTED;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {kUmBK, kUmBM};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SKV_OK : SKV_ERR_INVALID_ARG;
+}
+}  // namespace
+
+extern "C" {
 
 int skv_ctx_means(const skv_ctx_map* map, const int16_t* d_q_even, uint64_t n_even, const float* d_mu_odd,
                   uint64_t n_odd, uint32_t n_coef, float* d_mu_out, void* d_scratch, uint64_t scratch_bytes,
-                  void* stream) {
-  if (!map || !map->d_V || !map->d_U) return SKV_ERR_INVALID_ARG;
+                  uint32_t* d_status, void* stream) {
+  if (!map || !map->d_V || !map->d_U || !d_status) return SKV_ERR_INVALID_ARG;
   const uint32_t R = map->rank, C = n_coef;
   if (R == 0 || R % 32 || R > 16384 || C == 0 || C % 32 || C > 16384 || map->shift1 > 30 || map->shift2 > 30)
     return SKV_ERR_INVALID_ARG;
-  if (n_odd > n_even || n_odd > 65535ull * kGemmBM) return SKV_ERR_INVALID_ARG;   // grid rows
+  if (n_odd > n_even || n_odd > 65535ull * kUmBM) return SKV_ERR_INVALID_ARG;   // grid rows
   if (n_odd == 0) return SKV_OK;
   if (!d_q_even || !d_mu_odd || !d_mu_out || !d_scratch || !aligned16(d_q_even) || !aligned16(d_mu_odd) ||
       !aligned16(d_mu_out) || !aligned16(d_scratch) || !aligned16(map->d_V) || !aligned16(map->d_U))
     return SKV_ERR_INVALID_ARG;
   if (scratch_bytes < skv_ctx_scratch_bytes(n_odd, C, R)) return SKV_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  __nv_bfloat16* X = static_cast<__nv_bfloat16*>(d_scratch);
-  __nv_bfloat16* G = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(d_scratch) + align256(n_odd * C * 2));
-  const uint64_t nx = n_odd * C;
+  uint8_t* sp = static_cast<uint8_t*>(d_scratch);
+  __nv_bfloat16* X = reinterpret_cast<__nv_bfloat16*>(sp);
+  __nv_bfloat16* G = reinterpret_cast<__nv_bfloat16*>(sp + align256(n_odd * C * 2));
+  __nv_bfloat16* Vb = reinterpret_cast<__nv_bfloat16*>(sp + align256(n_odd * C * 2) + align256(n_odd * R * 2));
+  __nv_bfloat16* Ub = Vb + align256((uint64_t)R * C * 2) / 2;
+  CUtensorMap tx, tv, tg, tu;
+  int st = make_tmap(&tx, X, C, n_odd);
+  if (st == SKV_OK) st = make_tmap(&tv, Vb, C, R);
+  if (st == SKV_OK) st = make_tmap(&tg, G, R, n_odd);
+  if (st == SKV_OK) st = make_tmap(&tu, Ub, R, C);
+  if (st != SKV_OK) return st;
+  static bool attr_set = false;   // idempotent; racing first calls set the same value
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(k_ctx_umma<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kUmSmem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(k_ctx_umma<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kUmSmem) !=
+            cudaSuccess)
+      return SKV_ERR_CUDA;
+    attr_set = true;
+  }
+  st = cuda_status(cudaMemsetAsync(d_status, 0, 4, s));
+  if (st != SKV_OK) return st;
+  const uint64_t nx = n_odd * C, nw = (uint64_t)R * C;
   k_ctx_x<<<(unsigned)((nx + 255) / 256), 256, 0, s>>>(d_q_even, n_even, n_odd, C, X);
-  const unsigned gm = (unsigned)((n_odd + kGemmBM - 1) / kGemmBM);
-  k_ctx_gemm<0><<<dim3((R + kGemmBN - 1) / kGemmBN, gm), 256, 0, s>>>(X, map->d_V, (uint32_t)n_odd, R, C,
-                                                                        map->shift1, G, nullptr, nullptr);
-  k_ctx_gemm<1><<<dim3((C + kGemmBN - 1) / kGemmBN, gm), 256, 0, s>>>(G, map->d_U, (uint32_t)n_odd, C, R,
-                                                                        map->shift2, nullptr, d_mu_odd, d_mu_out);
+  k_ctx_w<<<(unsigned)((nw + 255) / 256), 256, 0, s>>>(map->d_V, nw, Vb);
+  k_ctx_w<<<(unsigned)((nw + 255) / 256), 256, 0, s>>>(map->d_U, nw, Ub);
+  const unsigned gm = (unsigned)((n_odd + kUmBM - 1) / kUmBM);
+  k_ctx_umma<0><<<dim3((R + kUmBN - 1) / kUmBN, gm), 128, kUmSmem, s>>>(tx, tv, (uint32_t)n_odd, R, C, map->shift1,
+                                                                         G, nullptr, nullptr, d_status);
+  k_ctx_umma<1><<<dim3((C + kUmBN - 1) / kUmBN, gm), 128, kUmSmem, s>>>(tg, tu, (uint32_t)n_odd, C, R, map->shift2,
+                                                                         nullptr, d_mu_odd, d_mu_out, d_status);
   return launch_check();
 }
 

@@ -109,7 +109,7 @@ _SIGS = {
                                    C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
     "skv_ctx_scratch_bytes": (C.c_uint64, [C.c_uint64, C.c_uint32, C.c_uint32]),
     "skv_ctx_means": (C.c_int, [_CM, C.c_void_p, C.c_uint64, C.c_void_p, C.c_uint64, C.c_uint32, C.c_void_p,
-                                C.c_void_p, C.c_uint64, C.c_void_p]),
+                                C.c_void_p, C.c_uint64, C.c_void_p, C.c_void_p]),
 }
 
 
@@ -227,11 +227,11 @@ def skv_ctx_scratch_bytes(n_odd: int, n_coef: int, rank: int) -> int:
     return lib().skv_ctx_scratch_bytes(n_odd, n_coef, rank)
 
 
-def skv_ctx_means(cmap, q_even, n_even, mu_odd, n_odd, n_coef, mu_out, scratch, scratch_bytes=None,
+def skv_ctx_means(cmap, q_even, n_even, mu_odd, n_odd, n_coef, mu_out, scratch, status, scratch_bytes=None,
                   stream=None) -> int:
     nb = scratch_bytes if scratch_bytes is not None else scratch.numel() * scratch.element_size()
     return lib().skv_ctx_means(C.byref(cmap), _ptr(q_even), n_even, _ptr(mu_odd), n_odd, n_coef, _ptr(mu_out),
-                               _ptr(scratch), nb, _stream(stream))
+                               _ptr(scratch), nb, _ptr(status), _stream(stream))
 
 
 # --- paged pools (same names as the C ABI) -----------------------------------------------------

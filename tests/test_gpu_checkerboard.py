@@ -29,9 +29,12 @@ def _gpu_ctx(nat, V, U, s1, s2, qe, mo):
     out = torch.full_like(md, float("nan"))
     nb = nat.skv_ctx_scratch_bytes(mo.shape[0], qe.shape[1], V.shape[0])
     scratch = torch.empty(max(nb, 256), dtype=torch.uint8, device="cuda")
-    st = nat.skv_ctx_means(nat.ctx_map(Vd, Ud, s1, s2), qd, qe.shape[0], md, mo.shape[0], qe.shape[1], out, scratch)
+    status = torch.ones(4, dtype=torch.int32, device="cuda")
+    st = nat.skv_ctx_means(nat.ctx_map(Vd, Ud, s1, s2), qd, qe.shape[0], md, mo.shape[0], qe.shape[1], out, scratch,
+                           status)
     assert st == nat.SKV_OK
     torch.cuda.synchronize()
+    assert nat.skv_read_status(status) == nat.SKV_OK
     return out.cpu().numpy()
 
 
@@ -69,8 +72,10 @@ def test_two_pass_round_trip(nat):
     C = qe.shape[1]
     scratch = torch.empty(nat.skv_ctx_scratch_bytes(qo.shape[0], C, V.shape[0]), dtype=torch.uint8, device="cuda")
     cmap = nat.ctx_map(V, U, s1, s2)
+    status = torch.ones(4, dtype=torch.int32, device="cuda")
     mo2 = torch.empty_like(mo)
-    assert nat.skv_ctx_means(cmap, qe, qe.shape[0], mo, qo.shape[0], C, mo2, scratch) == nat.SKV_OK
+    assert nat.skv_ctx_means(cmap, qe, qe.shape[0], mo, qo.shape[0], C, mo2, scratch, status) == nat.SKV_OK
+    assert nat.skv_read_status(status) == nat.SKV_OK
     ce, ne = _coef_gpu(nat, w, qe, me, beta)
     co, no = _coef_gpu(nat, w, qo, mo2, beta)
     # the streams equal the oracle's
@@ -88,7 +93,8 @@ def test_two_pass_round_trip(nat):
     ce.decode(me, qe_d)
     assert ce.check() == nat.SKV_OK and torch.equal(qe_d, qe)
     mo3 = torch.empty_like(mo)
-    assert nat.skv_ctx_means(cmap, qe_d, qe.shape[0], mo, qo.shape[0], C, mo3, scratch) == nat.SKV_OK
+    assert nat.skv_ctx_means(cmap, qe_d, qe.shape[0], mo, qo.shape[0], C, mo3, scratch, status) == nat.SKV_OK
+    assert nat.skv_read_status(status) == nat.SKV_OK
     qo_d = torch.zeros_like(qo)
     co.decode(mo3, qo_d)
     assert co.check() == nat.SKV_OK and torch.equal(qo_d, qo)
@@ -101,7 +107,10 @@ def test_full_size_sampled_rows(nat):
     C, n_o = qe.shape[1], qo.shape[0]
     scratch = torch.empty(nat.skv_ctx_scratch_bytes(n_o, C, V.shape[0]), dtype=torch.uint8, device="cuda")
     mo2 = torch.empty_like(mo)
-    assert nat.skv_ctx_means(nat.ctx_map(V, U, s1, s2), qe, qe.shape[0], mo, n_o, C, mo2, scratch) == nat.SKV_OK
+    status = torch.ones(4, dtype=torch.int32, device="cuda")
+    assert nat.skv_ctx_means(nat.ctx_map(V, U, s1, s2), qe, qe.shape[0], mo, n_o, C, mo2, scratch,
+                             status) == nat.SKV_OK
+    assert nat.skv_read_status(status) == nat.SKV_OK
     Vh, Uh = V.cpu().numpy(), U.cpu().numpy()
     for t in [0, 1, 4095, 9999, n_o - 2, n_o - 1]:
         want = oracle.ctx_means(Vh, Uh, s1, s2, qe[t:t + 2].cpu().numpy(), mo[t:t + 1].cpu().numpy())
@@ -112,7 +121,7 @@ def test_ctx_rejects_bad_shapes(nat):
     V = torch.zeros((64, 100), dtype=torch.int8, device="cuda")
     U = torch.zeros((100, 64), dtype=torch.int8, device="cuda")
     z = torch.zeros(4096, dtype=torch.float32, device="cuda")
-    st = nat.skv_ctx_means(nat.ctx_map(V, U, 6, 8), z, 2, z, 2, 100, z, z)   # n_coef not a multiple of 32
+    st = nat.skv_ctx_means(nat.ctx_map(V, U, 6, 8), z, 2, z, 2, 100, z, z, z)   # n_coef not a multiple of 32
     assert st == nat.SKV_ERR_INVALID_ARG
-    st = nat.skv_ctx_means(nat.ctx_map(V[:, :96], U[:96], 6, 8), z, 1, z, 2, 96, z, z)   # more odd than even rows
+    st = nat.skv_ctx_means(nat.ctx_map(V[:, :96], U[:96], 6, 8), z, 1, z, 2, 96, z, z, z)   # more odd than even rows
     assert st == nat.SKV_ERR_INVALID_ARG
