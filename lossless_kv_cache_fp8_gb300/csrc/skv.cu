@@ -1420,10 +1420,18 @@ __global__ void __launch_bounds__(256) k_decode_coef(CodecArgs a) {
 // every partial sum stays below K * 127 * 8 < 2^24 for K <= 16384 (checked on
 // the host), so any summation order gives the same integer.
 // ---------------------------------------------------------------------------
-constexpr uint32_t kUmBM = 128, kUmBN = 128, kUmBK = 64;   // output tile and k-block (64 bf16 = 128 B rows)
-constexpr uint32_t kUmStages = 4;                            // k-blocks in flight
-constexpr uint32_t kUmTile = kUmBM * kUmBK * 2;              // one operand tile: 16 KB
-constexpr uint32_t kUmSmem = kUmStages * 2 * kUmTile + 1024 + 256;
+constexpr uint32_t kUmBM = 128, kUmBK = 64;   // output tile rows and k-block (64 bf16 = 128 B rows)
+#ifndef SKV_UM_BN
+#define SKV_UM_BN 128
+#endif
+constexpr uint32_t kUmBN = SKV_UM_BN;                        // output tile columns
+constexpr uint32_t kUmStages = kUmBN == 128 ? 3 : 4;         // k-blocks in flight
+constexpr uint32_t kUmCtas = kUmBN == 128 ? 2 : 1;           // CTAs per SM
+constexpr uint32_t kUmTileA = kUmBM * kUmBK * 2, kUmTileB = kUmBN * kUmBK * 2;
+constexpr uint32_t kUmStage = kUmTileA + kUmTileB;
+constexpr uint32_t kUmOutPitch = kUmBN + 4;                  // staged output row (32-bit words)
+static_assert(kUmBM * kUmOutPitch * 4 <= kUmStages * kUmStage, "output staging fits in the stages");
+constexpr uint32_t kUmSmem = kUmStages * kUmStage + 1024 + 256;
 // instruction descriptor (kind::f16): fp32 accumulator (bits 4-5 = 1), bf16 A
 // and B (bits 7-9, 10-12 = 1), both K-major, N / 8 at bit 17, M / 16 at bit 24
 constexpr uint32_t kUmIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((kUmBN >> 3) << 17) | ((kUmBM >> 4) << 24);
@@ -1498,14 +1506,29 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__global__ void __launch_bounds__(256) k_ctx_x(const int16_t* qe, uint64_t n_even, uint64_t n_odd, uint32_t C,
-                                              __nv_bfloat16* X) {
-  const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n_odd * C) return;
-  const uint64_t t = i / C, c = i - t * C;
-  int v = qe[t * C + c] + (t + 1 < n_even ? qe[(t + 1) * C + c] : 0);
-  v = v < -127 ? -127 : (v > 127 ? 127 : v);
-  X[i] = __int2bfloat16_rn(v);
+// x rows as bf16: block t builds row t, eight coefficients per thread and step
+__global__ void __launch_bounds__(256) k_ctx_x(const int16_t* qe, uint64_t n_even, uint32_t C, __nv_bfloat16* X) {
+  const uint64_t t = blockIdx.x;
+  const bool next = t + 1 < n_even;
+  const int16_t* r0 = qe + t * C;
+  const int16_t* r1 = r0 + C;
+  __nv_bfloat16* xr = X + t * C;
+  for (uint32_t j = threadIdx.x * 8; j < C; j += blockDim.x * 8) {
+    const uint4 a = *reinterpret_cast<const uint4*>(r0 + j);
+    const uint4 b = next ? *reinterpret_cast<const uint4*>(r1 + j) : make_uint4(0, 0, 0, 0);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      int lo = (int)(int16_t)(aw[k] & 0xFFFFu) + (int)(int16_t)(bw[k] & 0xFFFFu);
+      int hi = (int)(int16_t)(aw[k] >> 16) + (int)(int16_t)(bw[k] >> 16);
+      lo = lo < -127 ? -127 : (lo > 127 ? 127 : lo);
+      hi = hi < -127 ? -127 : (hi > 127 ? 127 : hi);
+      const __nv_bfloat162 h = __halves2bfloat162(__int2bfloat16_rn(lo), __int2bfloat16_rn(hi));
+      o[k] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(xr + j) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
 }
 // map factor entries, clamped to [-8, 8], as bf16 operands
 __global__ void __launch_bounds__(256) k_ctx_w(const int8_t* w, uint64_t n, __nv_bfloat16* wb) {
@@ -1517,21 +1540,23 @@ __global__ void __launch_bounds__(256) k_ctx_w(const int8_t* w, uint64_t n, __nv
 }
 
 // Out[M][N] = epilogue(A[M][K] . B[N][K]^T), A and B bf16 row-major (K-major),
-// one 128 x 128 output tile per CTA on the 5th-generation tensor cores:
-// thread 0 streams k-blocks of both operands into a 4-deep ring of
-// shared-memory stages with tile loads, thread 32 issues the MMAs into a
-// 128 x 128 fp32 accumulator in tensor memory and releases each stage when its
-// MMAs complete, then all four warps read the accumulator rows back (warp w:
-// rows 32w..32w+31).  Rows past M and k past K load as zeros.
+// one 128 x kUmBN output tile per CTA on the 5th-generation tensor cores:
+// thread 0 streams k-blocks of both operands into a ring of shared-memory
+// stages with tile loads, thread 32 issues the MMAs into a 128 x kUmBN fp32
+// accumulator in tensor memory and releases each stage when its MMAs
+// complete.  The four warps then move the accumulator rows (warp w: rows
+// 32w..32w+31) through shared memory, as floor(acc / 2^s), so that each row
+// of the output is written (and, EPI 1, mu read) by a whole warp at once.
+// Rows past M and k past K load as zeros.
 // EPI 0: G = bf16(clamp(floor(acc / 2^s), +-127));  EPI 1: mu' from mu and
 // floor(acc / 2^s).  N is a multiple of 32 (checked on the host).
 template <int EPI>
-__global__ void __launch_bounds__(128, 1) k_ctx_umma(const __grid_constant__ CUtensorMap tmA,
-                                                     const __grid_constant__ CUtensorMap tmB, uint32_t M, uint32_t N,
-                                                     uint32_t K, uint32_t s, __nv_bfloat16* G, const float* mu,
-                                                     float* out, uint32_t* status) {
+__global__ void __launch_bounds__(128, kUmCtas) k_ctx_umma(const __grid_constant__ CUtensorMap tmA,
+                                                           const __grid_constant__ CUtensorMap tmB, uint32_t M,
+                                                           uint32_t N, uint32_t K, uint32_t s, __nv_bfloat16* G,
+                                                           const float* mu, float* out, uint32_t* status) {
   const uint32_t base = (smem_addr(g_smem) + 1023u) & ~1023u;   // stages need 1024-byte alignment
-  const uint32_t bar_full = base + kUmStages * 2 * kUmTile;
+  const uint32_t bar_full = base + kUmStages * kUmStage;
   const uint32_t bar_empty = bar_full + 8 * kUmStages;
   const uint32_t bar_done = bar_empty + 8 * kUmStages;
   const uint32_t tslot = bar_done + 8;
@@ -1564,10 +1589,10 @@ __global__ void __launch_bounds__(128, 1) k_ctx_umma(const __grid_constant__ CUt
         ok = false;
         break;
       }
-      const uint32_t dst = base + st * 2 * kUmTile;
-      mbar_expect_tx(bar_full + 8 * st, 2 * kUmTile);
+      const uint32_t dst = base + st * kUmStage;
+      mbar_expect_tx(bar_full + 8 * st, kUmStage);
       tma_load_2d(dst, &tmA, kb * kUmBK, m0, bar_full + 8 * st);
-      tma_load_2d(dst + kUmTile, &tmB, kb * kUmBK, n0, bar_full + 8 * st);
+      tma_load_2d(dst + kUmTileA, &tmB, kb * kUmBK, n0, bar_full + 8 * st);
     }
   } else if (threadIdx.x == 32) {
     for (uint32_t kb = 0; kb < nk; ++kb) {
@@ -1577,7 +1602,7 @@ __global__ void __launch_bounds__(128, 1) k_ctx_umma(const __grid_constant__ CUt
         break;
       }
       tc_fence_after();
-      const uint64_t da = umma_desc(base + st * 2 * kUmTile), db = umma_desc(base + st * 2 * kUmTile + kUmTile);
+      const uint64_t da = umma_desc(base + st * kUmStage), db = umma_desc(base + st * kUmStage + kUmTileA);
 #pragma unroll
       for (uint32_t k = 0; k < kUmBK / 16; ++k)        // 16 bf16 = 32 bytes along the swizzled row
         umma_bf16(tmem, da + 2 * k, db + 2 * k, (kb | k) != 0);
@@ -1588,51 +1613,76 @@ __global__ void __launch_bounds__(128, 1) k_ctx_umma(const __grid_constant__ CUt
   __syncwarp();
   if (!mbar_wait(bar_done, 0)) ok = false;
   tc_fence_after();
-  const uint32_t row = m0 + warp * 32 + lane;
+  // accumulator rows -> floor(acc / 2^s) in the (now idle) stages, row r at r * kUmOutPitch words
+  const uint32_t srow = base + (warp * 32 + lane) * kUmOutPitch * 4;
 #pragma unroll 1
   for (uint32_t c0 = 0; c0 < kUmBN; c0 += 32) {
     uint32_t r[32];
     tmem_ld32(tmem + ((warp * 32u) << 16) + c0, r);
-    const uint32_t n = n0 + c0;
-    if (row >= M || n >= N) continue;
-    const uint64_t o = (uint64_t)row * N + n;
-    if (EPI == 0) {
-      uint32_t h[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        int v0 = (int)__uint_as_float(r[2 * j]) >> s, v1 = (int)__uint_as_float(r[2 * j + 1]) >> s;
-        v0 = v0 < -127 ? -127 : (v0 > 127 ? 127 : v0);
-        v1 = v1 < -127 ? -127 : (v1 > 127 ? 127 : v1);
-        const __nv_bfloat162 b = __halves2bfloat162(__int2bfloat16_rn(v0), __int2bfloat16_rn(v1));
-        h[j] = *reinterpret_cast<const uint32_t*>(&b);
-      }
-      uint4* dst = reinterpret_cast<uint4*>(G + o);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) dst[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
-    } else {
-      const float4* src = reinterpret_cast<const float4*>(mu + o);
-      float4* dst = reinterpret_cast<float4*>(out + o);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float4 m4 = src[j];
-        const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
-        float res[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          int mm;
-          uint32_t ff;
-          coef_mean(mv[u], &mm, &ff);
-          long long q = 16ll * mm + ff + ((int)__uint_as_float(r[4 * j + u]) >> s);
-          q = q < -8388607 ? -8388607 : (q > 8388607 ? 8388607 : q);
-          res[u] = (float)q / 16.0f;
-        }
-        dst[j] = make_float4(res[0], res[1], res[2], res[3]);
-      }
+    for (int j = 0; j < 32; j += 4) {
+      const int v0 = (int)__uint_as_float(r[j]) >> s, v1 = (int)__uint_as_float(r[j + 1]) >> s;
+      const int v2 = (int)__uint_as_float(r[j + 2]) >> s, v3 = (int)__uint_as_float(r[j + 3]) >> s;
+      asm volatile("st.shared.v4.s32 [%0], {%1, %2, %3, %4};" ::"r"(srow + (c0 + j) * 4), "r"(v0), "r"(v1), "r"(v2),
+                   "r"(v3)
+                   : "memory");
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kUmBN));
+  // rows out: warp w takes rows w, w + 4, ...; lane l columns 4l..4l+3 (+128);
+  // eight rows per step, so that their mu loads are in flight together
+  constexpr uint32_t kRows = 8;
+#pragma unroll 1
+  for (uint32_t r0 = warp; r0 < kUmBM; r0 += 4 * kRows) {
+#pragma unroll
+    for (uint32_t c = lane * 4; c < kUmBN; c += 128) {
+      const uint32_t n = n0 + c;
+      if (n >= N) continue;
+      float4 m4[kRows];
+      if (EPI == 1) {
+#pragma unroll
+        for (uint32_t i = 0; i < kRows; ++i) {
+          const uint32_t row = m0 + r0 + 4 * i;
+          m4[i] = row < M ? *reinterpret_cast<const float4*>(mu + (uint64_t)row * N + n) : make_float4(0, 0, 0, 0);
+        }
+      }
+#pragma unroll
+      for (uint32_t i = 0; i < kRows; ++i) {
+        const uint32_t rr = r0 + 4 * i, row = m0 + rr;
+        if (row >= M) continue;
+        int v[4];
+        asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+                     : "r"(base + (rr * kUmOutPitch + c) * 4)
+                     : "memory");
+        const uint64_t o = (uint64_t)row * N + n;
+        if (EPI == 0) {
+          int w[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) w[u] = v[u] < -127 ? -127 : (v[u] > 127 ? 127 : v[u]);
+          const __nv_bfloat162 h0 = __halves2bfloat162(__int2bfloat16_rn(w[0]), __int2bfloat16_rn(w[1]));
+          const __nv_bfloat162 h1 = __halves2bfloat162(__int2bfloat16_rn(w[2]), __int2bfloat16_rn(w[3]));
+          *reinterpret_cast<uint2*>(G + o) =
+              make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+        } else {
+          const float mv[4] = {m4[i].x, m4[i].y, m4[i].z, m4[i].w};
+          float res[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            int mm;
+            uint32_t ff;
+            coef_mean(mv[u], &mm, &ff);
+            int q = 16 * mm + (int)ff + v[u];      // |16 mm + ff| < 2^26, |v| < 2^24: no overflow
+            q = q < -8388607 ? -8388607 : (q > 8388607 ? 8388607 : q);
+            res[u] = (float)q * 0.0625f;
+          }
+          *reinterpret_cast<float4*>(out + o) = make_float4(res[0], res[1], res[2], res[3]);
+        }
+      }
+    }
+  }
   if (!ok) atomicOr(status, SKV_FLAG_TIMEOUT);
 }
 
@@ -2130,12 +2180,12 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
 }
 // bf16 matrix [rows][inner] (row pitch inner * 2 bytes) read in 128-row x 64-column
 // boxes in the 128-byte swizzle; out-of-range elements read as zero
-int make_tmap(CUtensorMap* tm, const void* ptr, uint64_t inner, uint64_t rows) {
+int make_tmap(CUtensorMap* tm, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows) {
   const PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
   if (!enc) return SKV_ERR_UNSUPPORTED;
   const cuuint64_t dims[2] = {inner, rows};
   const cuuint64_t strides[1] = {inner * 2};
-  const cuuint32_t box[2] = {kUmBK, kUmBM};
+  const cuuint32_t box[2] = {kUmBK, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -2166,10 +2216,10 @@ int skv_ctx_means(const skv_ctx_map* map, const int16_t* d_q_even, uint64_t n_ev
   __nv_bfloat16* Vb = reinterpret_cast<__nv_bfloat16*>(sp + align256(n_odd * C * 2) + align256(n_odd * R * 2));
   __nv_bfloat16* Ub = Vb + align256((uint64_t)R * C * 2) / 2;
   CUtensorMap tx, tv, tg, tu;
-  int st = make_tmap(&tx, X, C, n_odd);
-  if (st == SKV_OK) st = make_tmap(&tv, Vb, C, R);
-  if (st == SKV_OK) st = make_tmap(&tg, G, R, n_odd);
-  if (st == SKV_OK) st = make_tmap(&tu, Ub, R, C);
+  int st = make_tmap(&tx, X, C, n_odd, kUmBM);
+  if (st == SKV_OK) st = make_tmap(&tv, Vb, C, R, kUmBN);
+  if (st == SKV_OK) st = make_tmap(&tg, G, R, n_odd, kUmBM);
+  if (st == SKV_OK) st = make_tmap(&tu, Ub, R, C, kUmBN);
   if (st != SKV_OK) return st;
   static bool attr_set = false;   // idempotent; racing first calls set the same value
   if (!attr_set) {
@@ -2182,8 +2232,8 @@ int skv_ctx_means(const skv_ctx_map* map, const int16_t* d_q_even, uint64_t n_ev
   }
   st = cuda_status(cudaMemsetAsync(d_status, 0, 4, s));
   if (st != SKV_OK) return st;
-  const uint64_t nx = n_odd * C, nw = (uint64_t)R * C;
-  k_ctx_x<<<(unsigned)((nx + 255) / 256), 256, 0, s>>>(d_q_even, n_even, n_odd, C, X);
+  const uint64_t nw = (uint64_t)R * C;
+  k_ctx_x<<<(unsigned)n_odd, 256, 0, s>>>(d_q_even, n_even, C, X);
   k_ctx_w<<<(unsigned)((nw + 255) / 256), 256, 0, s>>>(map->d_V, nw, Vb);
   k_ctx_w<<<(unsigned)((nw + 255) / 256), 256, 0, s>>>(map->d_U, nw, Ub);
   const unsigned gm = (unsigned)((n_odd + kUmBM - 1) / kUmBM);
