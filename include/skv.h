@@ -90,8 +90,13 @@ extern "C" {
  *   SKV_TABLE_FREQ_OFF 256 x u16: frequencies (sum 4096, each >= 1)
  *   SKV_TABLE_CUM_OFF  257 x u16: cumulative frequencies (cum[256] = 4096)
  * KV streams have 32 tables (scale bin b = table b); COEF streams have 1024
- * (table 16*b + f: scale bin b, mean fraction f/16). */
+ * (table 16*b + f: scale bin b, mean fraction f/16).  A COEF blob continues,
+ * at n_tables * SKV_TABLE_STRIDE, with SKV_TABLE_SLOT_BYTES per table: 4096 x
+ * u32 slot entries sym | fr << 8 | (slot - cum) << 20 (the slot's symbol, its
+ * frequency and the slot's offset within it: one read per decoding step for
+ * tables that stay in L2).  skv_tables_bytes gives the whole blob's size. */
 #define SKV_TABLE_STRIDE 8704u
+#define SKV_TABLE_SLOT_BYTES 16384u
 #define SKV_TABLE_ENC_OFF 0u
 #define SKV_TABLE_LUT_OFF 2048u
 #define SKV_TABLE_DEC_OFF 6144u
@@ -150,7 +155,7 @@ uint64_t skv_num_channels(const skv_params* p);  /* entries of the bins array   
 uint32_t skv_num_tables(const skv_params* p);    /* 32 (KV) or 1024 (COEF)         */
 uint64_t skv_num_chunks(const skv_params* p);
 uint64_t skv_num_lanes(const skv_params* p);     /* lane_offsets has n_lanes + 1   */
-uint64_t skv_tables_bytes(const skv_params* p);  /* num_tables * SKV_TABLE_STRIDE  */
+uint64_t skv_tables_bytes(const skv_params* p);  /* num_tables * SKV_TABLE_STRIDE (+ slot entries, COEF) */
 uint64_t skv_max_bitstream_bytes(const skv_params* p); /* worst case of any input  */
 uint64_t skv_encode_workspace_bytes(const skv_params* p);
 

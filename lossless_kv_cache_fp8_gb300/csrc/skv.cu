@@ -606,6 +606,9 @@ __global__ void __launch_bounds__(256) k_build_tables(uint8_t* blob, uint32_t su
       if (cums[mid] <= slot) lo = mid; else hi = mid;
     }
     lut[slot] = (uint8_t)lo;
+    if (coef)
+      reinterpret_cast<uint32_t*>(blob + (uint64_t)gridDim.x * SKV_TABLE_STRIDE + (uint64_t)t * SKV_TABLE_SLOT_BYTES)[slot] =
+          lo | ((cums[lo + 1] - cums[lo]) << 8) | ((slot - cums[lo]) << 20);
   }
 }
 
@@ -1307,47 +1310,130 @@ __device__ __forceinline__ void coef_mean(float mu, int* m, uint32_t* f) {
   *f = (uint32_t)mq & 15u;
 }
 
+// The 8 positions of a group: q and mu as read from memory (vectors when the
+// group is whole; loaded one group ahead of their use), then per position the
+// mean split, the table and whether the position is coded (skip: components
+// switched off, bin 0xFF, and positions past the slice end).
+struct CoefRaw {
+  float4 m0, m1;
+  uint4 q;
+};
+struct CoefGroup {
+  int m[8];
+  uint32_t tbl[8];
+  int16_t q[8];
+  uint32_t skip;
+};
+__device__ __forceinline__ void coef_load(const CodecArgs& a, uint64_t p0, uint32_t ne, bool with_q, CoefRaw& R) {
+  const int16_t* q = reinterpret_cast<const int16_t*>(a.tgt);
+  const float* mu = reinterpret_cast<const float*>(a.prd);
+  if (ne == 8) {
+    R.m0 = __ldg(reinterpret_cast<const float4*>(mu + p0));
+    R.m1 = __ldg(reinterpret_cast<const float4*>(mu + p0) + 1);
+    R.q = with_q ? __ldg(reinterpret_cast<const uint4*>(q + p0)) : make_uint4(0, 0, 0, 0);
+    return;
+  }
+  float mv[8];
+  uint32_t qw[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    mv[e] = (uint32_t)e < ne ? __ldg(mu + p0 + e) : 0.f;
+    if (with_q && (uint32_t)e < ne) qw[e >> 1] |= (uint32_t)(uint16_t)__ldg(q + p0 + e) << (16 * (e & 1));
+  }
+  R.m0 = make_float4(mv[0], mv[1], mv[2], mv[3]);
+  R.m1 = make_float4(mv[4], mv[5], mv[6], mv[7]);
+  R.q = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+}
+__device__ __forceinline__ void coef_group(const CodecArgs& a, uint64_t p0, uint32_t ne, const CoefRaw& R,
+                                           CoefGroup& G) {
+  const float mv[8] = {R.m0.x, R.m0.y, R.m0.z, R.m0.w, R.m1.x, R.m1.y, R.m1.z, R.m1.w};
+  const uint32_t qw[4] = {R.q.x, R.q.y, R.q.z, R.q.w};
+  uint32_t c = (uint32_t)(p0 % a.C);
+  G.skip = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    G.q[e] = (int16_t)(qw[e >> 1] >> (16 * (e & 1)));
+    const uint32_t bin = (uint32_t)e < ne ? __ldg(a.bins + c) : 0xFFu;
+    c = c + 1 == a.C ? 0 : c + 1;
+    uint32_t f;
+    coef_mean(mv[e], &G.m[e], &f);
+    G.tbl[e] = 16u * bin + f;
+    if (bin == 0xFFu) G.skip |= 1u << e;
+    else if (bin > 63u) { atomicOr(a.status, SKV_FLAG_BAD_BIN); G.tbl[e] = 1023; }
+  }
+}
+
+// One coding step where do_it holds; elsewhere x and the stream are left alone
+// (the entry must still be a valid one: the step is computed, then dropped).
+__device__ __forceinline__ void enc_step_gmem_if(uint32_t& x, uint16_t*& wp, uint2 e, bool do_it) {
+  const bool ren = do_it && x >= (e.y & 0xFFF00000u);
+  if (ren) *(wp - 1) = (uint16_t)x;
+  wp -= ren ? 1 : 0;
+  const uint32_t xr = ren ? x >> 16 : x;
+  const uint32_t q = enc_quot(xr, e.x, e.y);
+  const uint32_t xn = xr + q * (4096u - (e.y >> 20)) + ((e.y >> 8) & 0xFFFu);
+  x = do_it ? xn : x;
+}
+
+// Groups of 8 positions go to the lanes in turn (group g of a chunk to lane
+// g mod 32).  A group's inputs are read one group ahead; its 8 table entries
+// are fetched before its steps so that their loads overlap.  Escapes take a
+// warp-uniform branch.  (Fetching the entries one group ahead as well, so that
+// their latency overlaps the previous group's steps, measured slower.)
 __global__ void __launch_bounds__(256) k_encode_coef(CodecArgs a) {
   const uint32_t lane = threadIdx.x & 31;
   const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
   const uint64_t chunk_pos = (uint64_t)kLanes * a.K;
-  const int16_t* q = reinterpret_cast<const int16_t*>(a.tgt);
-  const float* mu = reinterpret_cast<const float*>(a.prd);
+  const uint2* const encb = reinterpret_cast<const uint2*>(a.tables + SKV_TABLE_ENC_OFF);
+  constexpr uint32_t kEntStride = SKV_TABLE_STRIDE / 8;
   for (uint64_t chunk = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); chunk < a.n_chunks;
        chunk += warps) {
     const uint64_t first = chunk * chunk_pos;
     const uint64_t n_pos = min(chunk_pos, a.slice_pos - first);
     const uint32_t n_groups = (uint32_t)((n_pos + 7) / 8);
     const uint32_t n_g = lane < n_groups ? (n_groups - lane + 31) / 32 : 0;
+    const int n_iter = (int)((n_groups + 31) / 32);            // warp-uniform (lane 0 has the most)
     const uint64_t g = chunk * kLanes + lane;
     uint16_t* const slot_end = a.slots + (g + 1) * a.slot_words;
     uint16_t* wp = slot_end;
     uint32_t x = kStateLow;
-    for (int i = (int)n_g - 1; i >= 0; --i) {
-      const uint64_t p0 = first + ((uint64_t)i * 32 + lane) * 8;   // position of the group
-      const uint32_t ne = (uint32_t)min((uint64_t)8, first + n_pos - p0);
-      uint32_t c = (uint32_t)((p0 + ne - 1) % a.C);                 // component of the last element
-      for (int e = (int)ne - 1; e >= 0; --e) {
-        const uint32_t bin = a.bins[c];
-        const uint64_t pos = p0 + (uint32_t)e;
-        c = c == 0 ? a.C - 1 : c - 1;
-        if (bin == 0xFFu) continue;
-        int m;
-        uint32_t f;
-        coef_mean(__ldg(mu + pos), &m, &f);
-        const int r = (int)__ldg(q + pos) - m;
-        uint32_t sym = (uint32_t)(r + 127);
+    auto gpos = [&](int i) { return first + ((uint64_t)i * 32 + lane) * 8; };   // position of group i
+    auto gnum = [&](uint64_t p0) { return (uint32_t)min((uint64_t)8, first + n_pos - p0); };
+    CoefRaw R;
+    if (n_g) coef_load(a, gpos((int)n_g - 1), gnum(gpos((int)n_g - 1)), true, R);
+    for (int i = n_iter - 1; i >= 0; --i) {
+      const uint32_t act = __ballot_sync(0xFFFFFFFFu, i < (int)n_g);
+      if (i >= (int)n_g) continue;
+      const uint64_t p0 = gpos(i);
+      const uint32_t ne = gnum(p0);
+      CoefGroup G;
+      coef_group(a, p0, ne, R, G);
+      if (i > 0) coef_load(a, gpos(i - 1), gnum(gpos(i - 1)), true, R);
+      uint2 en[8];
+      uint32_t esc = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const bool d = !((G.skip >> e) & 1u);
+        uint32_t sym = (uint32_t)((int)G.q[e] - G.m[e] + 127);
         if (sym > 254u) {
-          const uint32_t raw = (uint32_t)r & 0xFFFFu;
-          enc_raw_gmem(x, wp, raw & 0xFFu);
-          enc_raw_gmem(x, wp, raw >> 8);
           sym = 255;
+          esc |= (d ? 1u : 0u) << e;
         }
-        uint32_t tbl = 16u * bin + f;
-        if (bin > 63u) { atomicOr(a.status, SKV_FLAG_BAD_BIN); tbl = 1023; }
-        const uint2 en = __ldg(reinterpret_cast<const uint2*>(a.tables + (uint64_t)tbl * SKV_TABLE_STRIDE +
-                                                              SKV_TABLE_ENC_OFF) + sym);
-        enc_step_gmem(x, wp, en);
+        en[e] = __ldg(encb + (d ? G.tbl[e] : 0u) * kEntStride + sym);
+      }
+      if (__any_sync(act, esc != 0)) {
+#pragma unroll
+        for (int e = 7; e >= 0; --e) {
+          if ((esc >> e) & 1u) {
+            const uint32_t raw = (uint32_t)((int)G.q[e] - G.m[e]) & 0xFFFFu;
+            enc_raw_gmem(x, wp, raw & 0xFFu);
+            enc_raw_gmem(x, wp, raw >> 8);
+          }
+          enc_step_gmem_if(x, wp, en[e], !((G.skip >> e) & 1u));
+        }
+      } else {
+#pragma unroll
+        for (int e = 7; e >= 0; --e) enc_step_gmem_if(x, wp, en[e], !((G.skip >> e) & 1u));
       }
     }
     *--wp = (uint16_t)x;
@@ -1356,51 +1442,62 @@ __global__ void __launch_bounds__(256) k_encode_coef(CodecArgs a) {
   }
 }
 
+// Decoding reads one slot entry per step (symbol, frequency and offset: see
+// the table layout), a dependent L2 read: the step chain is bound by its latency.
 __global__ void __launch_bounds__(256) k_decode_coef(CodecArgs a) {
   const uint32_t lane = threadIdx.x & 31;
   const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
   const uint64_t chunk_pos = (uint64_t)kLanes * a.K;
   int16_t* q = reinterpret_cast<int16_t*>(a.out);
-  const float* mu = reinterpret_cast<const float*>(a.prd);
+  const uint32_t* slot_tab = reinterpret_cast<const uint32_t*>(a.tables + (uint64_t)kCoefTables * SKV_TABLE_STRIDE);
   for (uint64_t chunk = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); chunk < a.n_chunks;
        chunk += warps) {
     const uint64_t first = chunk * chunk_pos;
     const uint64_t n_pos = min(chunk_pos, a.slice_pos - first);
     const uint32_t n_groups = (uint32_t)((n_pos + 7) / 8);
     const uint32_t n_g = lane < n_groups ? (n_groups - lane + 31) / 32 : 0;
+    const uint32_t n_iter = (n_groups + 31) / 32;              // warp-uniform
     const uint64_t g = chunk * kLanes + lane;
     uint64_t sa, sb;
     const bool ok = lane_span(a.offs, g, a.n_lanes, a.n_bytes, &sa, &sb);
     DecLane L;
     dec_open(L, a.bs, sa, sb, ok, a.status);
-    for (uint32_t i = 0; i < n_g; ++i) {
-      const uint64_t p0 = first + ((uint64_t)i * 32 + lane) * 8;
-      const uint32_t ne = (uint32_t)min((uint64_t)8, first + n_pos - p0);
-      uint32_t c = (uint32_t)(p0 % a.C);
-      for (uint32_t e = 0; e < ne; ++e) {
-        const uint32_t bin = a.bins[c];
-        const uint64_t pos = p0 + e;
-        c = c + 1 == a.C ? 0 : c + 1;
-        if (bin == 0xFFu) { q[pos] = 0; continue; }
-        int m;
-        uint32_t f;
-        coef_mean(__ldg(mu + pos), &m, &f);
-        uint32_t tbl = 16u * bin + f;
-        if (bin > 63u) { atomicOr(a.status, SKV_FLAG_BAD_BIN); tbl = 1023; }
-        const uint8_t* tb = a.tables + (uint64_t)tbl * SKV_TABLE_STRIDE;
-        const uint32_t slot = L.x & 4095u;
-        const uint32_t sym = __ldg(tb + SKV_TABLE_LUT_OFF + slot);
-        const uint32_t dv = __ldg(reinterpret_cast<const uint32_t*>(tb + SKV_TABLE_DEC_OFF) + sym);
-        L.x = (dv & 0xFFFFu) * (L.x >> 12) + slot - (dv >> 16);
-        dec_renorm(L);
-        uint32_t r;
-        if (sym == 255u) {
-          r = dec_raw(L);
-          r = (r << 8) | dec_raw(L);
-        } else {
-          r = (uint32_t)((int)sym - 127);
+    auto gpos = [&](uint32_t i) { return first + ((uint64_t)i * 32 + lane) * 8; };
+    auto gnum = [&](uint64_t p0) { return (uint32_t)min((uint64_t)8, first + n_pos - p0); };
+    CoefRaw R;
+    if (n_g) coef_load(a, gpos(0), gnum(gpos(0)), false, R);
+    for (uint32_t i = 0; i < n_iter; ++i) {
+      const uint32_t act = __ballot_sync(0xFFFFFFFFu, i < n_g);
+      if (i >= n_g) continue;
+      const uint64_t p0 = gpos(i);
+      const uint32_t ne = gnum(p0);
+      CoefGroup G;
+      coef_group(a, p0, ne, R, G);
+      if (i + 1 < n_g) coef_load(a, gpos(i + 1), gnum(gpos(i + 1)), false, R);
+      uint32_t qo[4] = {0, 0, 0, 0};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const bool d = !((G.skip >> e) & 1u);
+        const uint32_t se = __ldg(slot_tab + (d ? G.tbl[e] : 0u) * 4096u + (L.x & 4095u));
+        const uint32_t sym = se & 0xFFu;
+        const uint32_t xn = ((se >> 8) & 0xFFFu) * (L.x >> 12) + (se >> 20);
+        L.x = d ? xn : L.x;
+        dec_renorm(L);                    // a skipped position leaves x >= 2^16: no renormalisation
+        uint32_t r = (uint32_t)((int)sym - 127);
+        if (__any_sync(act, d && sym == 255u)) {
+          if (d && sym == 255u) {
+            r = dec_raw(L);
+            r = (r << 8) | dec_raw(L);
+          }
         }
-        q[pos] = (int16_t)(uint16_t)(((uint32_t)m + r) & 0xFFFFu);
+        qo[e >> 1] |= (d ? (((uint32_t)G.m[e] + r) & 0xFFFFu) : 0u) << (16 * (e & 1));
+      }
+      if (ne == 8) {
+        *reinterpret_cast<uint4*>(q + p0) = make_uint4(qo[0], qo[1], qo[2], qo[3]);
+      } else {
+#pragma unroll
+        for (uint32_t e = 0; e < 8; ++e)
+          if (e < ne) q[p0 + e] = (int16_t)(qo[e >> 1] >> (16 * (e & 1)));
       }
     }
     dec_close(L, a.status);
@@ -1865,7 +1962,8 @@ uint64_t skv_num_lanes(const skv_params* p) {
 }
 uint64_t skv_tables_bytes(const skv_params* p) {
   Geo g;
-  return make_geo(p, &g) == SKV_OK ? (uint64_t)g.n_tables * SKV_TABLE_STRIDE : 0;
+  if (make_geo(p, &g) != SKV_OK) return 0;
+  return (uint64_t)g.n_tables * (SKV_TABLE_STRIDE + (g.dtype == SKV_COEF_I16 ? SKV_TABLE_SLOT_BYTES : 0));
 }
 uint64_t skv_max_bitstream_bytes(const skv_params* p) {
   Geo g;
@@ -1918,8 +2016,7 @@ int skv_build_tables(const skv_params* p, void* d_tables, uint64_t tables_bytes,
   Geo g;
   int st = make_geo(p, &g);
   if (st != SKV_OK) return st;
-  if (!d_tables || !aligned16(d_tables) || tables_bytes < (uint64_t)g.n_tables * SKV_TABLE_STRIDE)
-    return SKV_ERR_INVALID_ARG;
+  if (!d_tables || !aligned16(d_tables) || tables_bytes < skv_tables_bytes(p)) return SKV_ERR_INVALID_ARG;
   k_build_tables<<<g.n_tables, 256, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<uint8_t*>(d_tables), g.sub, g.dtype == SKV_COEF_I16 ? 1 : 0);
   return launch_check();
@@ -2006,10 +2103,10 @@ static int encode_impl(const skv_params* p, const Paged* pg, const void* d_targe
     return SKV_OK;
   }
   {
+    // one warp per CTA: the few long lanes of a coefficient stream spread evenly over the SMs
     int sms = sm_count();
-    uint64_t nb = (g.n_chunks + 7) / 8;
-    uint64_t cap_blocks = (uint64_t)(sms > 0 ? sms : 1) * 8;
-    k_encode_coef<<<(unsigned)(nb < cap_blocks ? nb : cap_blocks), 256, 0, s>>>(a);
+    const uint64_t cap_blocks = (uint64_t)(sms > 0 ? sms : 1) * 32;
+    k_encode_coef<<<(unsigned)(g.n_chunks < cap_blocks ? g.n_chunks : cap_blocks), 32, 0, s>>>(a);
   }
   if ((st = launch_check()) != SKV_OK) return st;
   unsigned long long* part = reinterpret_cast<unsigned long long*>(ws + wl.part_off);
@@ -2069,10 +2166,10 @@ static int decode_impl(const skv_params* p, const Paged* pg, const void* d_bitst
   a.D = g.D;
   a.C = g.C;
   if (g.dtype == SKV_COEF_I16) {
+    // one warp per CTA: the few long lanes of a coefficient stream spread evenly over the SMs
     int sms = sm_count();
-    uint64_t nb = (g.n_chunks + 7) / 8;
-    uint64_t cap_blocks = (uint64_t)(sms > 0 ? sms : 1) * 8;
-    k_decode_coef<<<(unsigned)(nb < cap_blocks ? nb : cap_blocks), 256, 0, s>>>(a);
+    const uint64_t cap_blocks = (uint64_t)(sms > 0 ? sms : 1) * 32;
+    k_decode_coef<<<(unsigned)(g.n_chunks < cap_blocks ? g.n_chunks : cap_blocks), 32, 0, s>>>(a);
     return launch_check();
   }
   int blocks, threads;

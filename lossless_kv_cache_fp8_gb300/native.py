@@ -22,6 +22,7 @@ SKV_FP8_E4M3, SKV_BF16, SKV_COEF_I16 = 1, 2, 3
 SKV_TABLE_STRIDE = 8704
 SKV_TABLE_ENC_OFF, SKV_TABLE_LUT_OFF, SKV_TABLE_DEC_OFF = 0, 2048, 6144
 SKV_TABLE_FREQ_OFF, SKV_TABLE_CUM_OFF = 7168, 7680
+SKV_TABLE_SLOT_BYTES = 16384
 
 
 class SkvError(RuntimeError):

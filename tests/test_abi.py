@@ -42,7 +42,8 @@ def test_sizes_match_oracle_geometry(lib, name):
     assert s["channels"] == g["n_channels"] and s["tables"] == g["n_tables"]
     assert s["positions"] == w.n_positions
     assert s["max_bitstream"] >= 2 * g["n_lanes"] * 2
-    assert s["tables_bytes"] == s["tables"] * native.SKV_TABLE_STRIDE
+    slot = native.SKV_TABLE_SLOT_BYTES if w.dtype == synth.COEF else 0
+    assert s["tables_bytes"] == s["tables"] * (native.SKV_TABLE_STRIDE + slot)
 
 
 def test_param_validation(lib):

@@ -151,6 +151,17 @@ def test_table_blob_structures(nat, kind):
         assert np.array_equal(dec, (f | (c[:256] << 16)).astype(np.uint32))
         lut = blob[t, nat.SKV_TABLE_LUT_OFF:nat.SKV_TABLE_LUT_OFF + 4096]
         assert np.array_equal(lut, np.repeat(np.arange(256), f).astype(np.uint8))
+    if kind == "coef":
+        # slot entries after the tables: symbol | fr << 8 | (slot - cum) << 20
+        nt = blob.shape[0]
+        raw = codec.tables.cpu().numpy()
+        assert raw.size == nt * (nat.SKV_TABLE_STRIDE + nat.SKV_TABLE_SLOT_BYTES)
+        se = raw[nt * nat.SKV_TABLE_STRIDE:].copy().view(np.uint32).reshape(nt, 4096).astype(np.int64)
+        slots = np.arange(4096)
+        for t in range(nt):
+            sym = np.repeat(np.arange(256), fr[t].astype(np.int64))
+            want = sym | (fr[t].astype(np.int64)[sym] << 8) | ((slots - cum[t].astype(np.int64)[sym]) << 20)
+            assert np.array_equal(se[t], want), t
 
 
 FULL_EXACT = ["qwen3-0.6b-1k-fp8", "hybrid-coef-32k-x2048"]

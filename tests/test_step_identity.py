@@ -62,7 +62,7 @@ def _header_defines():
 
 def test_binding_constants_match_header():
     h = _header_defines()
-    names = ["SKV_TABLE_STRIDE", "SKV_TABLE_ENC_OFF", "SKV_TABLE_LUT_OFF", "SKV_TABLE_DEC_OFF",
+    names = ["SKV_TABLE_STRIDE", "SKV_TABLE_SLOT_BYTES", "SKV_TABLE_ENC_OFF", "SKV_TABLE_LUT_OFF", "SKV_TABLE_DEC_OFF",
              "SKV_TABLE_FREQ_OFF", "SKV_TABLE_CUM_OFF", "SKV_OK", "SKV_ERR_INVALID_ARG", "SKV_ERR_CUDA",
              "SKV_ERR_CAPACITY", "SKV_ERR_CORRUPT", "SKV_ERR_TIMEOUT", "SKV_ERR_UNSUPPORTED",
              "SKV_FP8_E4M3", "SKV_BF16", "SKV_COEF_I16"]
