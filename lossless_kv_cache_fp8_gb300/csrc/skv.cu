@@ -295,15 +295,7 @@ __device__ __forceinline__ void enc_raw_smem_if(uint32_t& x, uint32_t& rp, uint3
   const uint32_t xn = ((xr >> 4) << 12) | (xr & 15u) | (v << 4);
   x = do_it ? xn : x;
 }
-// the same with words written downward straight into global scratch (COEF path)
-__device__ __forceinline__ void enc_step_gmem(uint32_t& x, uint16_t*& wp, uint2 e) {
-  if (x >= (e.y & 0xFFF00000u)) {
-    *--wp = (uint16_t)x;
-    x >>= 16;
-  }
-  const uint32_t q = enc_quot(x, e.x, e.y);
-  x = x + q * (4096u - (e.y >> 20)) + ((e.y >> 8) & 0xFFFu);
-}
+// a raw byte as a uniform step, words written downward straight into global scratch (COEF path)
 __device__ __forceinline__ void enc_raw_gmem(uint32_t& x, uint16_t*& wp, uint32_t v) {
   if (x >= (1u << 24)) {
     *--wp = (uint16_t)x;
@@ -1518,12 +1510,9 @@ __global__ void __launch_bounds__(256) k_decode_coef(CodecArgs a) {
 // the host), so any summation order gives the same integer.
 // ---------------------------------------------------------------------------
 constexpr uint32_t kUmBM = 128, kUmBK = 64;   // output tile rows and k-block (64 bf16 = 128 B rows)
-#ifndef SKV_UM_BN
-#define SKV_UM_BN 128
-#endif
-constexpr uint32_t kUmBN = SKV_UM_BN;                        // output tile columns
-constexpr uint32_t kUmStages = kUmBN == 128 ? 3 : 4;         // k-blocks in flight
-constexpr uint32_t kUmCtas = kUmBN == 128 ? 2 : 1;           // CTAs per SM
+constexpr uint32_t kUmBN = 128;                              // output tile columns
+constexpr uint32_t kUmStages = 3;                            // k-blocks in flight
+constexpr uint32_t kUmCtas = 2;                              // CTAs per SM (one's epilogue overlaps the other's MMAs)
 constexpr uint32_t kUmTileA = kUmBM * kUmBK * 2, kUmTileB = kUmBN * kUmBK * 2;
 constexpr uint32_t kUmStage = kUmTileA + kUmTileB;
 constexpr uint32_t kUmOutPitch = kUmBN + 4;                  // staged output row (32-bit words)
