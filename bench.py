@@ -462,8 +462,8 @@ def paged_run(args, w, codec, tgt, prd, stream, total, peak):
 def checkerboard_run(args, w, stream, dev):
     """The coefficient stream split by token parity with the checkerboard context:
     even rows coded with their means, odd rows with the context-shifted means
-    (skv_ctx_means: two tcgen05 tensor-core products); decode = even rows, context,
-    odd rows.  Reports the context call's tensor throughput and the ratio
+    (skv_ctx_means: two tcgen05 tensor-core products), the two parities on two
+    streams; decode = even rows, context, odd rows.  Reports the context call's tensor throughput and the ratio
     against coding the odd rows with their token-conditioned means alone."""
     import torch
     from lossless_kv_cache_fp8_gb300 import native, synth
@@ -493,10 +493,15 @@ def checkerboard_run(args, w, stream, dev):
     del co_plain
     qe_d, qo_d = torch.empty_like(qe), torch.empty_like(qo)
 
+    # the two parities encode concurrently: the odd rows' context needs only q_even
+    side = torch.cuda.Stream(dev)
+
     def enc():
-        ce.encode(qe, me, want_total=False)
+        side.wait_stream(stream)
+        ce.encode(qe, me, want_total=False, stream=side)
         ctx(qe)
         co.encode(qo, mo2, want_total=False)
+        stream.wait_stream(side)
 
     def dec():
         ce.decode(me, qe_d)

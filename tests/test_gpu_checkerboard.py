@@ -38,7 +38,8 @@ def _gpu_ctx(nat, V, U, s1, s2, qe, mo):
     return out.cpu().numpy()
 
 
-@pytest.mark.parametrize("C,R,n_e,n_o", [(256, 64, 33, 33), (96, 32, 5, 4), (2048, 1024, 300, 300), (512, 1024, 131, 130)])
+@pytest.mark.parametrize("C,R,n_e,n_o", [(256, 64, 33, 33), (96, 32, 5, 4), (2048, 1024, 300, 300), (512, 1024, 131, 130),
+                                        (416, 160, 258, 257)])
 def test_ctx_means_match_oracle(nat, C, R, n_e, n_o):
     rng = np.random.default_rng(C + R + n_o)
     V = rng.integers(-8, 9, (R, C)).astype(np.int8)
