@@ -326,6 +326,14 @@ int skv_encode_noalloc(const skv_params* p, const void* d_target, const void* d_
 int skv_selftest_lookback(uint64_t* d_state, uint32_t n_chunks, uint32_t missing_chunk,
                           uint32_t max_spins, uint64_t* d_excl, uint32_t* d_status, void* stream);
 
+/* Self-test of the bounded waits of the tensor-core context products (no
+ * counterpart on the pages): launches one tile of the first product with its
+ * tile loads switched off, so that the MMA thread's wait for operands runs out
+ * after about a second; the kernel must then set SKV_FLAG_TIMEOUT in d_status,
+ * free its tensor memory and return.  d_scratch: 48 KB, 16-byte aligned,
+ * caller-owned (its contents are overwritten). */
+int skv_selftest_ctx_wait(void* d_scratch, uint32_t* d_status, void* stream);
+
 /* Synchronises the stream, reads the status word and returns SKV_OK or the
  * code of the most serious flag (CORRUPT > CAPACITY > TIMEOUT > INVALID_ARG
  * for an out-of-range bin or block-table entry). */

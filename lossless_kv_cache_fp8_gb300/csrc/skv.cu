@@ -1640,7 +1640,8 @@ template <int EPI>
 __global__ void __launch_bounds__(128, kUmCtas) k_ctx_umma(const __grid_constant__ CUtensorMap tmA,
                                                            const __grid_constant__ CUtensorMap tmB, uint32_t M,
                                                            uint32_t N, uint32_t K, uint32_t s, __nv_bfloat16* G,
-                                                           const float* mu, float* out, uint32_t* status) {
+                                                           const float* mu, float* out, uint32_t* status,
+                                                           uint32_t no_loads) {
   const uint32_t base = (smem_addr(g_smem) + 1023u) & ~1023u;   // stages need 1024-byte alignment
   const uint32_t bar_full = base + kUmStages * kUmStage;
   const uint32_t bar_empty = bar_full + 8 * kUmStages;
@@ -1668,7 +1669,7 @@ __global__ void __launch_bounds__(128, kUmCtas) k_ctx_umma(const __grid_constant
   uint32_t tmem;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem) : "r"(tslot) : "memory");
   bool ok = true;
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && !no_loads) {   // no_loads: self-test of the bounded waits (nothing arrives)
     for (uint32_t kb = 0; kb < nk; ++kb) {
       const uint32_t st = kb % kUmStages;
       if (kb >= kUmStages && !mbar_wait(bar_empty + 8 * st, ((kb / kUmStages) - 1) & 1)) {
@@ -2324,9 +2325,26 @@ int skv_ctx_means(const skv_ctx_map* map, const int16_t* d_q_even, uint64_t n_ev
   k_ctx_w<<<(unsigned)((nw + 255) / 256), 256, 0, s>>>(map->d_U, nw, Ub);
   const unsigned gm = (unsigned)((n_odd + kUmBM - 1) / kUmBM);
   k_ctx_umma<0><<<dim3((R + kUmBN - 1) / kUmBN, gm), 128, kUmSmem, s>>>(tx, tv, (uint32_t)n_odd, R, C, map->shift1,
-                                                                         G, nullptr, nullptr, d_status);
+                                                                         G, nullptr, nullptr, d_status, 0u);
   k_ctx_umma<1><<<dim3((C + kUmBN - 1) / kUmBN, gm), 128, kUmSmem, s>>>(tg, tu, (uint32_t)n_odd, C, R, map->shift2,
-                                                                         nullptr, d_mu_odd, d_mu_out, d_status);
+                                                                         nullptr, d_mu_odd, d_mu_out, d_status, 0u);
+  return launch_check();
+}
+
+int skv_selftest_ctx_wait(void* d_scratch, uint32_t* d_status, void* stream) {
+  if (!d_scratch || !aligned16(d_scratch) || !d_status) return SKV_ERR_INVALID_ARG;
+  // one 128 x 128 tile over a 128 x 64 bf16 operand in the scratch; no tile is ever loaded
+  __nv_bfloat16* A = static_cast<__nv_bfloat16*>(d_scratch);
+  __nv_bfloat16* G = A + kUmBM * kUmBK;
+  CUtensorMap ta;
+  int st = make_tmap(&ta, A, kUmBK, kUmBM, kUmBM);
+  if (st != SKV_OK) return st;
+  if (cudaFuncSetAttribute(k_ctx_umma<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kUmSmem) != cudaSuccess)
+    return SKV_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = cuda_status(cudaMemsetAsync(d_status, 0, 4, s));
+  if (st != SKV_OK) return st;
+  k_ctx_umma<0><<<1, 128, kUmSmem, s>>>(ta, ta, kUmBM, kUmBN, kUmBK, 0, G, nullptr, nullptr, d_status, 1u);
   return launch_check();
 }
 

@@ -98,6 +98,7 @@ _SIGS = {
                              C.c_void_p, C.c_void_p, C.c_void_p]),
     "skv_encode_noalloc": (C.c_int, [_P, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                      C.c_uint64, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
+    "skv_selftest_ctx_wait": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p]),
     "skv_selftest_lookback": (C.c_int, [C.c_void_p, C.c_uint32, C.c_uint32, C.c_uint32, C.c_void_p, C.c_void_p,
                                         C.c_void_p]),
     "skv_read_status": (C.c_int, [C.c_void_p, C.c_void_p]),
@@ -212,6 +213,10 @@ def skv_encode_noalloc(p, target, pred, tables, bins, bitstream, cap_bytes, lane
 def skv_decode(p, bitstream, n_bytes, lane_offsets, pred, tables, bins, target_out, status, stream=None) -> int:
     return lib().skv_decode(C.byref(p), _ptr(bitstream), n_bytes, _ptr(lane_offsets), _ptr(pred), _ptr(tables),
                             _ptr(bins), _ptr(target_out), _ptr(status), _stream(stream))
+
+
+def skv_selftest_ctx_wait(scratch, status, stream=None) -> int:
+    return lib().skv_selftest_ctx_wait(_ptr(scratch), _ptr(status), _stream(stream))
 
 
 def skv_selftest_lookback(state, n_chunks, missing_chunk, max_spins, excl, status, stream=None) -> int:

@@ -126,3 +126,23 @@ def test_ctx_rejects_bad_shapes(nat):
     assert st == nat.SKV_ERR_INVALID_ARG
     st = nat.skv_ctx_means(nat.ctx_map(V[:, :96], U[:96], 6, 8), z, 1, z, 2, 96, z, z, z)   # more odd than even rows
     assert st == nat.SKV_ERR_INVALID_ARG
+
+
+def test_ctx_wait_gives_up_without_hanging(nat):
+    """a tensor-core tile whose operands never arrive: its MMA thread stops waiting
+    after about a second, the call reports a timeout, and the context stays usable"""
+    import time
+    scratch = torch.zeros(48 * 1024 // 4, dtype=torch.int32, device="cuda")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    t0 = time.perf_counter()
+    assert nat.skv_selftest_ctx_wait(scratch, status) == nat.SKV_OK
+    st = nat.skv_read_status(status)
+    dt = time.perf_counter() - t0
+    assert st == nat.SKV_ERR_TIMEOUT and dt < 10.0
+    rng = np.random.default_rng(3)
+    V = rng.integers(-8, 9, (64, 96)).astype(np.int8)
+    U = rng.integers(-8, 9, (96, 64)).astype(np.int8)
+    qe = rng.integers(-300, 301, (9, 96)).astype(np.int16)
+    mo = (rng.standard_normal((8, 96)) * 50).astype(np.float32)
+    want = oracle.ctx_means(V, U, 6, 8, qe, mo)
+    assert np.array_equal(_gpu_ctx(nat, V, U, 6, 8, qe, mo).view(np.uint32), want.view(np.uint32))
