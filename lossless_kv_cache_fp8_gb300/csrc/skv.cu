@@ -2308,15 +2308,9 @@ int skv_ctx_means(const skv_ctx_map* map, const int16_t* d_q_even, uint64_t n_ev
   if (st == SKV_OK) st = make_tmap(&tg, G, R, n_odd, kUmBM);
   if (st == SKV_OK) st = make_tmap(&tu, Ub, R, C, kUmBN);
   if (st != SKV_OK) return st;
-  static bool attr_set = false;   // idempotent; racing first calls set the same value
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(k_ctx_umma<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kUmSmem) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(k_ctx_umma<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kUmSmem) !=
-            cudaSuccess)
-      return SKV_ERR_CUDA;
-    attr_set = true;
-  }
+  // the attribute is per device: set on every call (a host-side call, no launch)
+  if ((st = set_smem(k_ctx_umma<0>, (int)kUmSmem)) != SKV_OK || (st = set_smem(k_ctx_umma<1>, (int)kUmSmem)) != SKV_OK)
+    return st;
   st = cuda_status(cudaMemsetAsync(d_status, 0, 4, s));
   if (st != SKV_OK) return st;
   const uint64_t nw = (uint64_t)R * C;
@@ -2339,8 +2333,7 @@ int skv_selftest_ctx_wait(void* d_scratch, uint32_t* d_status, void* stream) {
   CUtensorMap ta;
   int st = make_tmap(&ta, A, kUmBK, kUmBM, kUmBM);
   if (st != SKV_OK) return st;
-  if (cudaFuncSetAttribute(k_ctx_umma<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kUmSmem) != cudaSuccess)
-    return SKV_ERR_CUDA;
+  if ((st = set_smem(k_ctx_umma<0>, (int)kUmSmem)) != SKV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = cuda_status(cudaMemsetAsync(d_status, 0, 4, s));
   if (st != SKV_OK) return st;
