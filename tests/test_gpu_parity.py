@@ -2,10 +2,9 @@
 
 Bit-exact comparisons (integer path): calibration bins / sums / histograms, every
 table's frequencies and cumulative frequencies, bitstream bytes, lane offsets and
-decoded caches.  Small shapes compare everything; the full-size workloads compare
-everything that the oracle finishes in seconds and otherwise sampled chunks (the
-oracle codes a chunk from that chunk's own data), plus decode(encode(x)) == x on
-the whole cache, which holds at any size.
+decoded caches.  Small shapes compare everything in one oracle call; the large
+full-size workloads compare every chunk with the oracle coding that chunk from its
+own data (in host threads), plus decode(encode(x)) == x on the whole cache.
 """
 import numpy as np
 import pytest
@@ -173,9 +172,12 @@ def test_full_size_bit_exact(nat, name):
     full_compare(nat, synth.WORKLOADS[name])
 
 
-def sampled_compare(nat, w, n_samples=6, seed=0):
-    """generate on the GPU, code the whole cache there, compare sampled chunks
-    (first, last and random ones) with the oracle coding those chunks"""
+def every_chunk_compare(nat, w):
+    """generate on the GPU, code the whole cache there, then check every slice's
+    bins and every chunk's words and lane lengths against the oracle coding that
+    chunk from its own data (host threads: the oracle's C calls release the GIL)"""
+    import concurrent.futures as cf
+    import os
     t, p, c = synth.gen_workload(w, "cuda")
     codec = nat.Codec(nat.params_for(w), bitstream_capacity=w.raw_bytes)
     codec.calibrate(t, c)
@@ -192,42 +194,51 @@ def sampled_compare(nat, w, n_samples=6, seed=0):
     fr, cum = oracle.build_tables(po)
     _, gfr, gcum = table_arrays(nat, codec)
     assert np.array_equal(gfr, fr) and np.array_equal(gcum, cum)
-    rng = np.random.default_rng(seed)
-    chunks = sorted({0, g["n_chunks"] - 1, *rng.integers(0, g["n_chunks"], n_samples).tolist()})
+    tn, pn = host_bits(t), host_bits(p)
+    del t, p, c
+    torch.cuda.empty_cache()
+    assert total % 2 == 0
+    bs = codec.bitstream[:total].cpu().numpy().view(np.uint16)
     offs = codec.lane_offsets.cpu().numpy().astype(np.int64)
     assert offs[0] == 0 and offs[-1] == total and np.all(np.diff(offs) >= 4)
-    tflat, pflat = t.view(-1), p.view(-1)
     gbins = codec.bins[: g["n_channels"]].cpu().numpy()
-    sp, cs = g["slice_positions"], 32 * w.lane_syms
-    D = w.head_dim
-    for ch in chunks:
-        sl, k = divmod(ch, g["chunks_per_slice"])
-        first = sl * sp + k * cs
-        n_pos = min(cs, sp - k * cs)
-        # calibration of this slice by the oracle, from the slice's own first tokens
-        ncal = min(w.n_calib, w.n_tokens)
+    sp, cps, cs, D = g["slice_positions"], g["chunks_per_slice"], 32 * w.lane_syms, w.head_dim
+    ncal = min(w.n_calib, w.n_tokens)
+    po1 = oracle.kv_params(w.dtype, 1, 1, 1, D, ncal, w.lane_syms, w.n_calib)
+
+    def slice_job(sl):
         s0 = sl * sp
-        po1 = oracle.kv_params(w.dtype, 1, 1, 1, D, ncal, w.lane_syms, w.n_calib)
-        b1, _, _ = oracle.calibrate(po1, host_bits(tflat[s0:s0 + ncal * D]), host_bits(pflat[s0:s0 + ncal * D]))
-        assert np.array_equal(gbins[sl * D:(sl + 1) * D], b1), f"bins of slice {sl}"
-        tc = host_bits(tflat[first:first + n_pos])
-        pc = host_bits(pflat[first:first + n_pos])
-        words, lw = oracle.encode_chunk(po, ch, fr, cum, gbins, tc, pc)
-        a, b = offs[32 * ch], offs[32 * ch + 32]
-        got = codec.bitstream[a:b].cpu().numpy().view(np.uint16)
-        assert np.array_equal(got, words), f"chunk {ch}"
-        assert np.array_equal(np.diff(offs[32 * ch:32 * ch + 33]) // 2, lw.astype(np.int64))
+        b1, _, _ = oracle.calibrate(po1, tn[s0:s0 + ncal * D], pn[s0:s0 + ncal * D])
+        if not np.array_equal(gbins[sl * D:(sl + 1) * D], b1):
+            return f"bins of slice {sl}"
+        for k in range(cps):
+            ch = sl * cps + k
+            first, n_pos = s0 + k * cs, min(cs, sp - k * cs)
+            words, lw = oracle.encode_chunk(po, ch, fr, cum, gbins, tn[first:first + n_pos], pn[first:first + n_pos])
+            a, b = offs[32 * ch], offs[32 * ch + 32]
+            if not np.array_equal(bs[a // 2:b // 2], words):
+                return f"chunk {ch}"
+            if not np.array_equal(np.diff(offs[32 * ch:32 * ch + 33]) // 2, lw.astype(np.int64)):
+                return f"lane lengths of chunk {ch}"
+        return None
+
+    with cf.ThreadPoolExecutor(os.cpu_count() or 4) as ex:
+        errs = [e for e in ex.map(slice_job, range(g["n_chunks"] // cps)) if e]
+    assert not errs, errs[:5]
     return codec, total
 
 
 @pytest.mark.parametrize("name", ["qwen3-0.6b-8k-bf16", "qwen3-8b-32k-fp8", "qwen3-32b-128k-fp8"])
-def test_full_size_sampled(nat, name):
+def test_full_size_every_chunk(nat, name):
+    """the three large workloads at full size: every byte of the stream and every
+    lane offset against the oracle (chunk by chunk), every slice's bins, and the
+    decoded cache equal to the input"""
     w = synth.WORKLOADS[name]
     free, _ = torch.cuda.mem_get_info()
     need = 2 * w.raw_bytes + w.raw_bytes + nat.sizes(nat.params_for(w))["workspace"] + w.raw_bytes
     if need > free:
         pytest.skip(f"needs {need / 1e9:.0f} GB of device memory, {free / 1e9:.0f} GB free")
-    codec, total = sampled_compare(nat, w)
+    codec, total = every_chunk_compare(nat, w)
     ratio = w.raw_bytes / (total + 4 * codec.sz["lanes"] + codec.sz["channels"] + 64)
     print(f"{name}: {w.raw_bytes / 1e9:.2f} GB -> {total / 1e9:.3f} GB, ratio {ratio:.3f}")
     del codec
