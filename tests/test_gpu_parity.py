@@ -172,14 +172,14 @@ def test_full_size_bit_exact(nat, name):
     full_compare(nat, synth.WORKLOADS[name])
 
 
-def every_chunk_compare(nat, w):
+def every_chunk_compare(nat, w, model=0):
     """generate on the GPU, code the whole cache there, then check every slice's
     bins and every chunk's words and lane lengths against the oracle coding that
     chunk from its own data (host threads: the oracle's C calls release the GIL)"""
     import concurrent.futures as cf
     import os
     t, p, c = synth.gen_workload(w, "cuda")
-    codec = nat.Codec(nat.params_for(w), bitstream_capacity=w.raw_bytes)
+    codec = nat.Codec(nat.params_for(w, model=model), bitstream_capacity=w.raw_bytes)
     codec.calibrate(t, c)
     codec.build_tables()
     total = codec.encode(t, p)
@@ -189,7 +189,8 @@ def every_chunk_compare(nat, w):
     assert codec.check() == nat.SKV_OK
     assert torch.equal(out, t)
     del out
-    po = oparams(w)
+    po = oracle.kv_params(w.dtype, w.n_layers, w.n_kv, w.n_heads, w.head_dim, w.n_tokens, w.lane_syms,
+                          w.n_calib, model=model)
     g = oracle.geometry(po)
     fr, cum = oracle.build_tables(po)
     _, gfr, gcum = table_arrays(nat, codec)
@@ -204,7 +205,7 @@ def every_chunk_compare(nat, w):
     gbins = codec.bins[: g["n_channels"]].cpu().numpy()
     sp, cps, cs, D = g["slice_positions"], g["chunks_per_slice"], 32 * w.lane_syms, w.head_dim
     ncal = min(w.n_calib, w.n_tokens)
-    po1 = oracle.kv_params(w.dtype, 1, 1, 1, D, ncal, w.lane_syms, w.n_calib)
+    po1 = oracle.kv_params(w.dtype, 1, 1, 1, D, ncal, w.lane_syms, w.n_calib, model=model)
 
     def slice_job(sl):
         s0 = sl * sp
@@ -241,6 +242,20 @@ def test_full_size_every_chunk(nat, name):
     codec, total = every_chunk_compare(nat, w)
     ratio = w.raw_bytes / (total + 4 * codec.sz["lanes"] + codec.sz["channels"] + 64)
     print(f"{name}: {w.raw_bytes / 1e9:.2f} GB -> {total / 1e9:.3f} GB, ratio {ratio:.3f}")
+    del codec
+    torch.cuda.empty_cache()
+
+
+def test_full_size_every_chunk_exponent_model(nat):
+    """the 128K Qwen3-32B-shaped FP8 cache with the exponent residual model: every
+    chunk and every slice's base bins against the oracle"""
+    w = synth.WORKLOADS["qwen3-32b-128k-fp8"]
+    free, _ = torch.cuda.mem_get_info()
+    need = 2 * w.raw_bytes + w.raw_bytes + nat.sizes(nat.params_for(w))["workspace"] + w.raw_bytes
+    if need > free:
+        pytest.skip(f"needs {need / 1e9:.0f} GB of device memory, {free / 1e9:.0f} GB free")
+    codec, total = every_chunk_compare(nat, w, model=nat.SKV_MODEL_EXPONENT)
+    print(f"exponent model: {w.raw_bytes / 1e9:.2f} GB -> {total / 1e9:.3f} GB")
     del codec
     torch.cuda.empty_cache()
 
