@@ -1,6 +1,6 @@
 """Checkerboard context on the GPU (skv_ctx_means) against the oracle: the
 odd rows' shifted means bit for bit (small and full-width maps, ragged tiles,
-extreme values, weights outside [-8, 8]), sampled rows of the full 32K-token
+extreme values, weights outside [-8, 8]), every row of the full 32K-token
 stream, and the two-pass round trip through the COEF calls with streams equal
 to the oracle's."""
 import numpy as np
@@ -101,21 +101,33 @@ def test_two_pass_round_trip(nat):
     assert co.check() == nat.SKV_OK and torch.equal(qo_d, qo)
 
 
-def test_full_size_sampled_rows(nat):
+def test_full_size_every_row(nat):
+    """the full 32K-token stream's context (16384 odd rows, rank 1024): every odd
+    row's shifted means against the oracle (row blocks in host threads)"""
+    import concurrent.futures as cf
+    import os
     w = synth.WORKLOADS["hybrid-coef-32k-x2048"]
     qe, qo, me, mo, beta, V, U = synth.gen_coef_checkerboard(w, "cuda")
     s1, s2 = synth.CTX_SHIFT1, synth.CTX_SHIFT2
-    C, n_o = qe.shape[1], qo.shape[0]
+    C, n_e, n_o = qe.shape[1], qe.shape[0], qo.shape[0]
     scratch = torch.empty(nat.skv_ctx_scratch_bytes(n_o, C, V.shape[0]), dtype=torch.uint8, device="cuda")
     mo2 = torch.empty_like(mo)
     status = torch.ones(4, dtype=torch.int32, device="cuda")
-    assert nat.skv_ctx_means(nat.ctx_map(V, U, s1, s2), qe, qe.shape[0], mo, n_o, C, mo2, scratch,
+    assert nat.skv_ctx_means(nat.ctx_map(V, U, s1, s2), qe, n_e, mo, n_o, C, mo2, scratch,
                              status) == nat.SKV_OK
     assert nat.skv_read_status(status) == nat.SKV_OK
-    Vh, Uh = V.cpu().numpy(), U.cpu().numpy()
-    for t in [0, 1, 4095, 9999, n_o - 2, n_o - 1]:
-        want = oracle.ctx_means(Vh, Uh, s1, s2, qe[t:t + 2].cpu().numpy(), mo[t:t + 1].cpu().numpy())
-        assert np.array_equal(mo2[t:t + 1].cpu().numpy().view(np.uint32), want.view(np.uint32)), t
+    Vh, Uh, qh, mh = V.cpu().numpy(), U.cpu().numpy(), qe.cpu().numpy(), mo.cpu().numpy()
+    got = mo2.cpu().numpy().view(np.uint32)
+    step = 256
+
+    def block(t0):
+        t1 = min(t0 + step, n_o)
+        want = oracle.ctx_means(Vh, Uh, s1, s2, qh[t0:min(t1 + 1, n_e)], mh[t0:t1])
+        return t0 if not np.array_equal(got[t0:t1], want.view(np.uint32)) else None
+
+    with cf.ThreadPoolExecutor(os.cpu_count() or 4) as ex:
+        bad = [t for t in ex.map(block, range(0, n_o, step)) if t is not None]
+    assert not bad, f"row blocks {bad[:5]} differ"
 
 
 def test_ctx_rejects_bad_shapes(nat):
