@@ -117,3 +117,40 @@ def test_paged_bad_block_entry_is_flagged(nat):
     st, _ = nat.skv_encode_paged(prm, lay_bad, tp, pp, codec.tables, codec.bins, bs, codec.cap, off,
                                  codec.workspace, codec.workspace.numel(), status)
     assert st == nat.SKV_OK and nat.skv_read_status(status) == nat.SKV_ERR_INVALID_ARG
+
+
+def test_paged_full_size_equals_dense(nat):
+    """the 128K Qwen3-32B-shaped cache in 16-token pages: bins, stream and offsets
+    equal the dense call's (itself checked chunk by chunk against the oracle) and
+    decoding into the pool restores every target row"""
+    w = synth.WORKLOADS["qwen3-32b-128k-fp8"]
+    free, _ = torch.cuda.mem_get_info()
+    if free < 8 * w.raw_bytes:
+        pytest.skip(f"needs {8 * w.raw_bytes / 1e9:.0f} GB of device memory, {free / 1e9:.0f} GB free")
+    t, p, _ = synth.gen_workload(w, "cuda")
+    prm = nat.params_for(w)
+    codec = nat.Codec(prm, bitstream_capacity=w.raw_bytes)
+    codec.calibrate(t, p)
+    codec.build_tables()
+    total = codec.encode(t, p)
+    assert codec.check() == nat.SKV_OK
+    tp, pp, table, n_blocks = synth.to_paged(t, p, 16, seed=16)
+    del t, p
+    torch.cuda.empty_cache()
+    lay = nat.paged_layout(table, n_blocks, 16)
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    bins = torch.empty_like(codec.bins)
+    assert nat.skv_calibrate_paged(prm, lay, tp, pp, bins, status) == nat.SKV_OK
+    assert nat.skv_read_status(status) == nat.SKV_OK
+    nch = codec.sz["channels"]
+    assert torch.equal(bins[:nch], codec.bins[:nch])
+    bs = torch.full_like(codec.bitstream, 0xAB)
+    off = torch.full_like(codec.lane_offsets, -1)
+    st, n = nat.skv_encode_paged(prm, lay, tp, pp, codec.tables, bins, bs, codec.cap, off, codec.workspace,
+                                 codec.workspace.numel(), status)
+    assert st == nat.SKV_OK and nat.skv_read_status(status) == nat.SKV_OK
+    assert n == total and torch.equal(bs[:n], codec.bitstream[:n]) and torch.equal(off, codec.lane_offsets)
+    out = torch.zeros_like(tp)
+    assert nat.skv_decode_paged(prm, lay, bs, n, off, pp, codec.tables, bins, out, status) == nat.SKV_OK
+    assert nat.skv_read_status(status) == nat.SKV_OK
+    assert torch.equal(out, tp)
