@@ -1513,6 +1513,7 @@ constexpr uint32_t kUmBM = 128, kUmBK = 64;   // output tile rows and k-block (6
 constexpr uint32_t kUmBN = 128;                              // output tile columns
 constexpr uint32_t kUmStages = 3;                            // k-blocks in flight
 constexpr uint32_t kUmCtas = 2;                              // CTAs per SM (one's epilogue overlaps the other's MMAs)
+constexpr uint32_t kUmThreads = 256;                         // 8 warps: two per tensor-memory lane quarter
 constexpr uint32_t kUmTileA = kUmBM * kUmBK * 2, kUmTileB = kUmBN * kUmBK * 2;
 constexpr uint32_t kUmStage = kUmTileA + kUmTileB;
 constexpr uint32_t kUmOutPitch = kUmBN + 4;                  // staged output row (32-bit words)
@@ -1637,7 +1638,7 @@ __global__ void __launch_bounds__(256) k_ctx_w(const int8_t* w, uint64_t n, __nv
 // EPI 0: G = bf16(clamp(floor(acc / 2^s), +-127));  EPI 1: mu' from mu and
 // floor(acc / 2^s).  N is a multiple of 32 (checked on the host).
 template <int EPI>
-__global__ void __launch_bounds__(128, kUmCtas) k_ctx_umma(const __grid_constant__ CUtensorMap tmA,
+__global__ void __launch_bounds__(kUmThreads, kUmCtas) k_ctx_umma(const __grid_constant__ CUtensorMap tmA,
                                                            const __grid_constant__ CUtensorMap tmB, uint32_t M,
                                                            uint32_t N, uint32_t K, uint32_t s, __nv_bfloat16* G,
                                                            const float* mu, float* out, uint32_t* status,
@@ -1700,12 +1701,14 @@ __global__ void __launch_bounds__(128, kUmCtas) k_ctx_umma(const __grid_constant
   __syncwarp();
   if (!mbar_wait(bar_done, 0)) ok = false;
   tc_fence_after();
-  // accumulator rows -> floor(acc / 2^s) in the (now idle) stages, row r at r * kUmOutPitch words
-  const uint32_t srow = base + (warp * 32 + lane) * kUmOutPitch * 4;
+  // accumulator rows -> floor(acc / 2^s) in the (now idle) stages, row r at r * kUmOutPitch words;
+  // warp w reads rows 32 (w mod 4) .. (its tensor-memory lane quarter), columns of half w / 4
+  const uint32_t q4 = warp & 3, half = warp >> 2;
+  const uint32_t srow = base + (q4 * 32 + lane) * kUmOutPitch * 4;
 #pragma unroll 1
-  for (uint32_t c0 = 0; c0 < kUmBN; c0 += 32) {
+  for (uint32_t c0 = half * (kUmBN / 2); c0 < (half + 1) * (kUmBN / 2); c0 += 32) {
     uint32_t r[32];
-    tmem_ld32(tmem + ((warp * 32u) << 16) + c0, r);
+    tmem_ld32(tmem + ((q4 * 32u) << 16) + c0, r);
 #pragma unroll
     for (int j = 0; j < 32; j += 4) {
       const int v0 = (int)__uint_as_float(r[j]) >> s, v1 = (int)__uint_as_float(r[j + 1]) >> s;
@@ -1718,11 +1721,11 @@ __global__ void __launch_bounds__(128, kUmCtas) k_ctx_umma(const __grid_constant
   tc_fence_before();
   __syncthreads();
   if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kUmBN));
-  // rows out: warp w takes rows w, w + 4, ...; lane l columns 4l..4l+3 (+128);
+  // rows out: warp w takes rows w, w + 8, ...; lane l columns 4l..4l+3 (+128);
   // eight rows per step, so that their mu loads are in flight together
-  constexpr uint32_t kRows = 8;
+  constexpr uint32_t kRows = 8, kWarps = kUmThreads / 32;
 #pragma unroll 1
-  for (uint32_t r0 = warp; r0 < kUmBM; r0 += 4 * kRows) {
+  for (uint32_t r0 = warp; r0 < kUmBM; r0 += kWarps * kRows) {
 #pragma unroll
     for (uint32_t c = lane * 4; c < kUmBN; c += 128) {
       const uint32_t n = n0 + c;
@@ -1731,13 +1734,13 @@ __global__ void __launch_bounds__(128, kUmCtas) k_ctx_umma(const __grid_constant
       if (EPI == 1) {
 #pragma unroll
         for (uint32_t i = 0; i < kRows; ++i) {
-          const uint32_t row = m0 + r0 + 4 * i;
+          const uint32_t row = m0 + r0 + kWarps * i;
           m4[i] = row < M ? *reinterpret_cast<const float4*>(mu + (uint64_t)row * N + n) : make_float4(0, 0, 0, 0);
         }
       }
 #pragma unroll
       for (uint32_t i = 0; i < kRows; ++i) {
-        const uint32_t rr = r0 + 4 * i, row = m0 + rr;
+        const uint32_t rr = r0 + kWarps * i, row = m0 + rr;
         if (row >= M) continue;
         int v[4];
         asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];"
@@ -2318,9 +2321,9 @@ int skv_ctx_means(const skv_ctx_map* map, const int16_t* d_q_even, uint64_t n_ev
   k_ctx_w<<<(unsigned)((nw + 255) / 256), 256, 0, s>>>(map->d_V, nw, Vb);
   k_ctx_w<<<(unsigned)((nw + 255) / 256), 256, 0, s>>>(map->d_U, nw, Ub);
   const unsigned gm = (unsigned)((n_odd + kUmBM - 1) / kUmBM);
-  k_ctx_umma<0><<<dim3((R + kUmBN - 1) / kUmBN, gm), 128, kUmSmem, s>>>(tx, tv, (uint32_t)n_odd, R, C, map->shift1,
+  k_ctx_umma<0><<<dim3((R + kUmBN - 1) / kUmBN, gm), kUmThreads, kUmSmem, s>>>(tx, tv, (uint32_t)n_odd, R, C, map->shift1,
                                                                          G, nullptr, nullptr, d_status, 0u);
-  k_ctx_umma<1><<<dim3((C + kUmBN - 1) / kUmBN, gm), 128, kUmSmem, s>>>(tg, tu, (uint32_t)n_odd, C, R, map->shift2,
+  k_ctx_umma<1><<<dim3((C + kUmBN - 1) / kUmBN, gm), kUmThreads, kUmSmem, s>>>(tg, tu, (uint32_t)n_odd, C, R, map->shift2,
                                                                          nullptr, d_mu_odd, d_mu_out, d_status, 0u);
   return launch_check();
 }
@@ -2337,7 +2340,7 @@ int skv_selftest_ctx_wait(void* d_scratch, uint32_t* d_status, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = cuda_status(cudaMemsetAsync(d_status, 0, 4, s));
   if (st != SKV_OK) return st;
-  k_ctx_umma<0><<<1, 128, kUmSmem, s>>>(ta, ta, kUmBM, kUmBN, kUmBK, 0, G, nullptr, nullptr, d_status, 1u);
+  k_ctx_umma<0><<<1, kUmThreads, kUmSmem, s>>>(ta, ta, kUmBM, kUmBN, kUmBK, 0, G, nullptr, nullptr, d_status, 1u);
   return launch_check();
 }
 
