@@ -1513,7 +1513,7 @@ constexpr uint32_t kUmBM = 128, kUmBK = 64;   // output tile rows and k-block (6
 constexpr uint32_t kUmBN = 128;                              // output tile columns
 constexpr uint32_t kUmStages = 3;                            // k-blocks in flight
 constexpr uint32_t kUmCtas = 2;                              // CTAs per SM (one's epilogue overlaps the other's MMAs)
-constexpr uint32_t kUmThreads = 256;                         // 8 warps: two per tensor-memory lane quarter
+constexpr uint32_t kUmThreads = 512;                         // 16 warps: four per tensor-memory lane quarter
 constexpr uint32_t kUmTileA = kUmBM * kUmBK * 2, kUmTileB = kUmBN * kUmBK * 2;
 constexpr uint32_t kUmStage = kUmTileA + kUmTileB;
 constexpr uint32_t kUmOutPitch = kUmBN + 4;                  // staged output row (32-bit words)
@@ -1702,11 +1702,12 @@ __global__ void __launch_bounds__(kUmThreads, kUmCtas) k_ctx_umma(const __grid_c
   if (!mbar_wait(bar_done, 0)) ok = false;
   tc_fence_after();
   // accumulator rows -> floor(acc / 2^s) in the (now idle) stages, row r at r * kUmOutPitch words;
-  // warp w reads rows 32 (w mod 4) .. (its tensor-memory lane quarter), columns of half w / 4
-  const uint32_t q4 = warp & 3, half = warp >> 2;
+  // warp w reads rows 32 (w mod 4) .. (its tensor-memory lane quarter), columns of part w / 4
+  constexpr uint32_t kParts = kUmThreads / 128, kPartCols = kUmBN / kParts;
+  const uint32_t q4 = warp & 3, part = warp >> 2;
   const uint32_t srow = base + (q4 * 32 + lane) * kUmOutPitch * 4;
 #pragma unroll 1
-  for (uint32_t c0 = half * (kUmBN / 2); c0 < (half + 1) * (kUmBN / 2); c0 += 32) {
+  for (uint32_t c0 = part * kPartCols; c0 < (part + 1) * kPartCols; c0 += 32) {
     uint32_t r[32];
     tmem_ld32(tmem + ((q4 * 32u) << 16) + c0, r);
 #pragma unroll
