@@ -1049,7 +1049,23 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
         }
         esc = mx > 254u;
       }
-      if (__any_sync(act, esc)) {
+      if (ESZ == 2 && !PAGED && __any_sync(act, esc)) {
+        // BF16: ve / vo hold the exact residuals + 127 (32-bit lanes); escapes
+        // are common enough that the raw steps sit behind a vote per position
+        // (the paged variant keeps the path below: its extra registers would spill)
+        if (__any_sync(act, buf_top - rp > kRoomEsc)) emit_flush_sync(act, buf_top, rp, gp);
+#pragma unroll
+        for (int e = G - 1; e >= 0; --e) {
+          const uint32_t v = (e & 1) ? vo[e >> 1] : ve[e >> 1];
+          const bool e_j = v > 254u;
+          if (__any_sync(act, e_j)) {
+            const uint32_t raw = (v - 127u) & 0xFFFFu;
+            enc_raw_smem_if(x, rp, raw & 0xFFu, e_j);
+            enc_raw_smem_if(x, rp, raw >> 8, e_j);
+          }
+          enc_step_smem(x, rp, lds_u64(tb[e] + (e_j ? 255u : v) * 8u));
+        }
+      } else if ((ESZ == 1 || PAGED) && __any_sync(act, esc)) {
         // rare: exact residuals per position, raw steps where one escapes
         if (__any_sync(act, buf_top - rp > kRoomEsc)) emit_flush_sync(act, buf_top, rp, gp);
         uint32_t t4[4];
