@@ -1089,8 +1089,10 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
       } else {
         if (__any_sync(act, buf_top - rp > kRoomPlain)) emit_flush_sync(act, buf_top, rp, gp);
         uint32_t t4[4];
-#pragma unroll
-        for (int e = G - 1; e >= 0; --e) {
+        // entry of position e: its load is issued two steps before the
+        // renormalisation store of the step before it, so the store does not
+        // hold the load back
+        auto entry_addr = [&](int e) -> uint32_t {
           if (MODEL && (e & 3) == 3) model_exp_word(bw[e >> 2], word_of(pc, e >> 2), kEncTabStride, t4);
           // byte offset of the entry: 8 * symbol (the upper lane's shift
           // also drops the lower lane, whose value is below 2^13)
@@ -1101,7 +1103,15 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
           } else {
             so = ((e & 1) ? vo[e >> 1] : ve[e >> 1]) << 3;
           }
-          enc_step_smem(x, rp, lds_u64((MODEL ? t4[e & 3] : tb[e]) + so));
+          return (MODEL ? t4[e & 3] : tb[e]) + so;
+        };
+        uint2 ent[G];
+#pragma unroll
+        for (int e = G - 1; e >= G - 2; --e) ent[e] = lds_u64(entry_addr(e));
+#pragma unroll
+        for (int e = G - 1; e >= 0; --e) {
+          if (e - 2 >= 0) ent[e - 2] = lds_u64(entry_addr(e - 2));
+          enc_step_smem(x, rp, ent[e]);
         }
       }
       tc = tn;
