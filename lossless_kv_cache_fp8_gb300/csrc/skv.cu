@@ -311,7 +311,7 @@ struct DecLane {
 };
 __device__ __forceinline__ void dec_renorm(DecLane& L) {
   if (L.x < kStateLow) {
-    L.x = (L.x << 16) | L.nxt;
+    L.x = __byte_perm(L.x, L.nxt, 0x1054);   // (x << 16) | nxt (nxt < 2^16)
     ++L.p;
     L.nxt = L.p < L.n ? L.w[L.p] : 0u;
   }
@@ -388,7 +388,7 @@ __device__ __forceinline__ uint32_t ring_word(const RingLane& L, uint32_t p) {
 }
 __device__ __forceinline__ void ring_renorm(RingLane& L) {
   if (L.x < kStateLow) {
-    L.x = (L.x << 16) | L.nxt;
+    L.x = __byte_perm(L.x, L.nxt, 0x1054);   // (x << 16) | nxt in one PRMT (nxt < 2^16)
     L.p += 2;
     L.nxt = ring_word(L, L.p);
   }
@@ -399,7 +399,7 @@ __device__ __forceinline__ uint32_t ring_raw_if(RingLane& L, bool do_it) {
   const uint32_t xn = 16u * (L.x >> 12) + (slot & 15u);
   const bool ren = do_it && xn < kStateLow;
   const uint32_t pn = L.p + 2;
-  L.x = do_it ? (ren ? ((xn << 16) | L.nxt) : xn) : L.x;
+  L.x = do_it ? (ren ? __byte_perm(xn, L.nxt, 0x1054) : xn) : L.x;
   if (ren) {
     L.p = pn;
     L.nxt = ring_word(L, pn);
