@@ -10,26 +10,32 @@
 //   [DCKV] "DCKV compresses a hybrid language model's prompt KV cache with
 //          learned transform coding"
 //
-// Kernels (all integer; nothing here uses tensor cores because no stage is a
-// dense contraction -- the bound is HBM bandwidth and integer issue):
+// Kernels.  The codec is integer work bound by the SM's integer and
+// shared-memory pipes (HBM is the roofline); only the checkerboard context map
+// is a dense contraction and runs on the tensor cores:
 //   k_build_tables    one CTA per table: Q32 Taylor exp, power chain, masses,
 //                     largest-remainder frequencies, encoder reciprocals,
-//                     slot->symbol table
+//                     slot->symbol table (and, COEF, one-read slot entries)
 //   k_calibrate_kv    one CTA per (layer, kv, head) slice: exact sum |r| per
 //                     channel over the calibration tokens, warp reductions,
 //                     optional histograms, scale bins
-//   k_encode_kv       persistent warps, one chunk (32 lanes) per warp at a
-//                     time, 128-bit coalesced loads of both caches (each lane
-//                     owns 16-byte groups), encoder tables staged in shared
-//                     memory, reverse pass writing renormalisation words
-//                     downward into the lane's scratch slot
-//   k_scan_*          exclusive scan of lane lengths -> lane byte offsets
-//   k_compact         copies each lane's words from scratch into the stream
+//   k_encode_kv       persistent warps taking chunks (32 lanes) from a ticket,
+//                     128-bit coalesced loads of both caches (each lane owns
+//                     16-byte groups), encoder tables in shared memory, reverse
+//                     pass into per-lane shared-memory word buffers flushed to
+//                     the warp's scratch slots; each chunk is placed in the
+//                     stream by a decoupled look-back one chunk later
 //   k_decode_kv       persistent warps, slot->symbol and decoder tables in
-//                     shared memory, reconstruction fused in: ordinal of the
-//                     prediction + residual, inverse ordinal, 128-bit stores
-//   k_*_coef          the same for transform-coefficient streams (1024 tables
-//                     read through L1/L2; switched-off components skipped)
+//                     shared memory, per-lane stream rings filled by cp.async,
+//                     speculative FP8 groups, reconstruction fused in: ordinal
+//                     of the prediction + residual, inverse ordinal, 128-bit
+//                     stores
+//   k_*_coef          transform-coefficient streams (1024 tables read through
+//                     L1/L2; switched-off components carry no symbol), with
+//                     k_scan_* (lane lengths -> byte offsets) and k_compact
+//   k_ctx_*           checkerboard context: x rows and bf16 map factors, then
+//                     two tcgen05 products (TMA-fed, accumulators in tensor
+//                     memory)
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -685,7 +691,7 @@ __global__ void k_calibrate_coef(const float* beta, uint8_t* bins, uint32_t C) {
 }
 
 // ---------------------------------------------------------------------------
-// Encoder, KV caches.  Persistent warps; warp w takes chunks w, w + W, ...
+// Encoder, KV caches.  Persistent warps take chunks from an atomic ticket.
 // Lane l of a chunk owns 16-byte groups l, l + 32, ...; the reverse pass walks
 // them from the last group down, prefetching the next group's 128-bit loads.
 // ---------------------------------------------------------------------------
@@ -1657,9 +1663,10 @@ __global__ void __launch_bounds__(256) k_ctx_w(const int8_t* w, uint64_t n, __nv
 // thread 0 streams k-blocks of both operands into a ring of shared-memory
 // stages with tile loads, thread 32 issues the MMAs into a 128 x kUmBN fp32
 // accumulator in tensor memory and releases each stage when its MMAs
-// complete.  The four warps then move the accumulator rows (warp w: rows
-// 32w..32w+31) through shared memory, as floor(acc / 2^s), so that each row
-// of the output is written (and, EPI 1, mu read) by a whole warp at once.
+// complete.  The sixteen warps then move the accumulator (warp w: rows
+// 32 (w mod 4).., its tensor-memory lane quarter, 32 columns from 32 (w / 4))
+// through shared memory, as floor(acc / 2^s), so that each row of the output
+// is written (and, EPI 1, mu read) by a whole warp at once.
 // Rows past M and k past K load as zeros.
 // EPI 0: G = bf16(clamp(floor(acc / 2^s), +-127));  EPI 1: mu' from mu and
 // floor(acc / 2^s).  N is a multiple of 32 (checked on the host).
