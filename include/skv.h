@@ -81,12 +81,13 @@ extern "C" {
 /* Table blob: table t occupies SKV_TABLE_STRIDE bytes at t*SKV_TABLE_STRIDE.
  * Within a table:
  *   SKV_TABLE_ENC_OFF  256 x {u32 m_lo, u32 w}: encoder entries with
- *                      w = fr << 20 | cum << 8 | h << 7 | s, where
- *                      m = h*2^32 + m_lo = ceil(2^(32+s) / fr) and
- *                      floor(x / fr) = (umulhi(x, m_lo) + h*x) >> s
+ *                      w = fr << 20 | cum << 8 | 1 << 7 | s, s = ceil(log2 fr),
+ *                      where m = 2^32 + m_lo = ceil(2^(32+s) / fr) and
+ *                      floor(x / fr) = (umulhi(x, m_lo) + x) >> s
  *                      exactly for every state x < fr*2^20 the encoder meets
  *   SKV_TABLE_LUT_OFF  4096 x u8: symbol owning each 12-bit slot
- *   SKV_TABLE_DEC_OFF  256 x u32: fr | cum << 16
+ *   SKV_TABLE_DEC_OFF  256 x u32: fr | (-cum mod 2^16) << 16 (the upper half
+ *                      read as a signed 16-bit number is -cum)
  *   SKV_TABLE_FREQ_OFF 256 x u16: frequencies (sum 4096, each >= 1)
  *   SKV_TABLE_CUM_OFF  257 x u16: cumulative frequencies (cum[256] = 4096)
  * KV streams have 32 tables (scale bin b = table b); COEF streams have 1024

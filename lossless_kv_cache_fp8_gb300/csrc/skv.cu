@@ -269,15 +269,21 @@ __device__ __forceinline__ uint4 lds_u128(uint32_t a) { return *reinterpret_cast
 __device__ __forceinline__ void sts_u128(uint32_t a, uint4 v) { *reinterpret_cast<uint4*>(g_smem + a) = v; }
 __device__ __forceinline__ void stg_u128(void* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 
-// Encoder entry {m_lo, w}, w = fr << 20 | cum << 8 | h << 7 | s:
-// floor(x / fr) = (umulhi(x, m_lo) + (h ? x : 0)) >> s.
-// prmt with selector 0x8888 replicates the sign bit of byte 0 (= h) into a mask.
+// Encoder entry {m_lo, w}, w = fr << 20 | cum << 8 | 1 << 7 | s with
+// s = ceil(log2 fr): the reciprocal m = 2^32 + m_lo always has its top bit at
+// 2^32, so floor(x / fr) = (umulhi(x, m_lo) + x) >> s (one multiply-add and a
+// shift; the sum stays below 2^32 for x < fr 2^20).
 __device__ __forceinline__ uint32_t enc_quot(uint32_t x, uint32_t m_lo, uint32_t w) {
-  uint32_t hmask;
-  asm("prmt.b32 %0, %1, 0, 0x8888;" : "=r"(hmask) : "r"(w));
-  const uint32_t t = __umulhi(x, m_lo) + (x & hmask);
-  return __funnelshift_r(t, 0u, w);   // shift amount = w & 31 = s
+  return __funnelshift_r(__umulhi(x, m_lo) + x, 0u, w);   // shift amount = w & 31 = s
 }
+
+// Constants held in registers (they come from the kernel arguments), so that
+// the multiply-adds written with them stay on the FMA pipe: with literals the
+// compiler turns them into shifts and adds on the integer ALU pipe, which the
+// encoder's main loop keeps the busiest.
+struct PipeConsts {
+  uint32_t k4096, minus1, k2p20, k8;
+};
 
 // one coding step; renormalisation words go to a downward-growing buffer
 // addressed by rp (shared-window byte address)
@@ -289,6 +295,19 @@ __device__ __forceinline__ void enc_step_smem(uint32_t& x, uint32_t& rp, uint2 e
   }
   const uint32_t q = enc_quot(x, e.x, e.y);
   x = x + q * (4096u - (e.y >> 20)) + ((e.y >> 8) & 0xFFFu);
+}
+// The same step with the threshold fr << 20 and the multiplier 4096 - fr
+// formed on the FMA pipe (both come from the entry, read ahead of the step,
+// so the longer latency stays off the state's dependency chain).
+__device__ __forceinline__ void enc_step_smem_fma(uint32_t& x, uint32_t& rp, uint2 e, const PipeConsts& k) {
+  const uint32_t fr = e.y >> 20;
+  if (x >= fr * k.k2p20) {
+    rp -= 2;
+    sts_u16(rp, x);
+    x >>= 16;
+  }
+  const uint32_t q = enc_quot(x, e.x, e.y);
+  x = x + q * (fr * k.minus1 + k.k4096) + ((e.y >> 8) & 0xFFFu);
 }
 // raw byte v as a uniform step (fr 16, cum 16 v), taken only where do_it holds
 __device__ __forceinline__ void enc_raw_smem_if(uint32_t& x, uint32_t& rp, uint32_t v, bool do_it) {
@@ -573,26 +592,19 @@ __global__ void __launch_bounds__(256) k_build_tables(uint8_t* blob, uint32_t su
   reinterpret_cast<uint16_t*>(tb + SKV_TABLE_FREQ_OFF)[i] = (uint16_t)fr;
   reinterpret_cast<uint16_t*>(tb + SKV_TABLE_CUM_OFF)[i] = (uint16_t)cum;
   if (i == 255) reinterpret_cast<uint16_t*>(tb + SKV_TABLE_CUM_OFF)[256] = 4096;
-  // encoder reciprocal: the smallest shift s with m = ceil(2^(32+s)/fr) < 2^33
-  // such that floor(x m / 2^(32+s)) = floor(x / fr) for all x < fr 2^20
-  // (error term (fr 2^20 - 1)(m fr - 2^(32+s)) < 2^(32+s)) and x m < 2^64
-  uint32_t sh = 12;
-  uint64_t mm = 0;
-  for (uint32_t s2 = 0; s2 <= 12; ++s2) {
-    const uint64_t k = 1ull << (32 + s2);
-    const uint64_t m2 = (k + fr - 1) / fr;
-    const uint64_t x1 = ((uint64_t)fr << 20) - 1;
-    if (m2 < (1ull << 33) && x1 * (m2 * fr - k) < k && __umul64hi(x1, m2) == 0) {
-      sh = s2;
-      mm = m2;
-      break;
-    }
-  }
+  // encoder reciprocal: s = ceil(log2 fr), m = ceil(2^(32+s)/fr) in [2^32, 2^33).
+  // floor(x m / 2^(32+s)) = floor(x / fr) for all x < fr 2^20, since the error
+  // term (fr 2^20 - 1)(m fr - 2^(32+s)) < fr^2 2^20 <= 2^(32+s) for s <= 12,
+  // and x m < 2^64 there
+  uint32_t sh = 0;
+  while ((1u << sh) < fr) ++sh;
+  const uint64_t mm = ((1ull << (32 + sh)) + fr - 1) / fr;
   uint2 enc;
   enc.x = (uint32_t)mm;
-  enc.y = (fr << 20) | (cum << 8) | ((uint32_t)(mm >> 32) << 7) | sh;
+  enc.y = (fr << 20) | (cum << 8) | (1u << 7) | sh;
   reinterpret_cast<uint2*>(tb + SKV_TABLE_ENC_OFF)[i] = enc;
-  reinterpret_cast<uint32_t*>(tb + SKV_TABLE_DEC_OFF)[i] = fr | (cum << 16);
+  // decoder entry: fr, and -cum as a signed upper half (the update adds it)
+  reinterpret_cast<uint32_t*>(tb + SKV_TABLE_DEC_OFF)[i] = fr | ((0u - cum) << 16);
   __syncthreads();
   // slot -> symbol: the last symbol whose cum <= slot
   uint8_t* lut = tb + SKV_TABLE_LUT_OFF;
@@ -717,6 +729,7 @@ struct CodecArgs {
   uint64_t cap;
   uint64_t slot_warps;              // warps that own a slot set in the workspace
   Paged pg;                         // paged pools (pg.bt == nullptr: dense caches)
+  PipeConsts k;                     // 4096, 0xFFFFFFFF, 2^20, 8 (see PipeConsts)
 };
 
 template <int ESZ>
@@ -1102,14 +1115,12 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
           if (MODEL && (e & 3) == 3) model_exp_word(bw[e >> 2], word_of(pc, e >> 2), kEncTabStride, t4);
           // byte offset of the entry: 8 * symbol (the upper lane's shift
           // also drops the lower lane, whose value is below 2^13)
-          uint32_t so;
+          const uint32_t tbe = MODEL ? t4[e & 3] : tb[e];
           if (ESZ == 1) {
             const uint32_t v = (e & 1) ? vo[e >> 2] : ve[e >> 2];
-            so = (e & 2) ? (v >> 13) : ((v & 0xFFFFu) << 3);
-          } else {
-            so = ((e & 1) ? vo[e >> 1] : ve[e >> 1]) << 3;
+            return (e & 2) ? tbe + (v >> 13) : (v & 0xFFFFu) * a.k.k8 + tbe;   // lower lane: multiply-add
           }
-          return (MODEL ? t4[e & 3] : tb[e]) + so;
+          return tbe + (((e & 1) ? vo[e >> 1] : ve[e >> 1]) << 3);
         };
         uint2 ent[G];
 #pragma unroll
@@ -1117,7 +1128,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
 #pragma unroll
         for (int e = G - 1; e >= 0; --e) {
           if (e - 2 >= 0) ent[e - 2] = lds_u64(entry_addr(e - 2));
-          enc_step_smem(x, rp, ent[e]);
+          enc_step_smem_fma(x, rp, ent[e], a.k);
         }
       }
       tc = tn;
@@ -1162,7 +1173,8 @@ __global__ void k_selftest_lookback(unsigned long long* st, uint32_t n, uint32_t
 
 // ---------------------------------------------------------------------------
 // Decoder, KV caches, fused with reconstruction.  Each lane reads its words
-// through a shared-memory ring (refilled every SUB symbols), looks the slot
+// through a shared-memory ring (refilled once per FP8 group on the speculative
+// pass, every SUB symbols where escapes are decoded), looks the slot
 // up in the shared slot->symbol table, rebuilds the target from the
 // prediction's ordinal and stores whole 16-byte groups.
 // ---------------------------------------------------------------------------
@@ -1177,7 +1189,7 @@ __device__ __forceinline__ void dec_exact(RingLane& L, uint32_t tbe, uint32_t pw
   const uint32_t slot = L.x & 4095u;
   const uint32_t sym = lds_u8(tbe + slot);
   const uint32_t dv = lds_u32(tbe + 4096u + sym * 4u);
-  L.x = (dv & 0xFFFFu) * (L.x >> 12) + slot - (dv >> 16);
+  L.x = (dv & 0xFFFFu) * (L.x >> 12) + slot + (uint32_t)((int32_t)dv >> 16);   // + (-cum)
   ring_renorm(L);
   uint32_t term = sym;
   // escapes are rare: a warp-uniform test keeps their steps off the common
@@ -1263,16 +1275,19 @@ __global__ void __launch_bounds__(dec_threads(PAGED, MODEL), 1) k_decode_kv(Code
       if (ESZ == 1) {
         // FP8: the group's 16 positions are decoded assuming no escape; if
         // any lane met one, those lanes decode the group again from the saved
-        // state (ring reloaded from the stream) with escapes handled.
+        // state (ring reloaded from the stream) with escapes handled.  Without
+        // raw steps a position consumes at most one word, so the 16 positions
+        // read at most 32 bytes: one refill at the group's start keeps the
+        // ring ahead of them.
         const uint32_t x0 = L.x, p0 = L.p, n0 = L.nxt;
         bool esc = false;
 #pragma unroll
         for (int e = 0; e < G; ++e) {
-          if (e % SUB == 0) ring_refill(L, act);
+          if (e == 0) ring_refill(L, act);
           const uint32_t slot = L.x & 4095u;
           const uint32_t sym = lds_u8(tb[e] + slot);
           const uint32_t dv = lds_u32(tb[e] + 4096u + sym * 4u);
-          L.x = (dv & 0xFFFFu) * (L.x >> 12) + slot - (dv >> 16);
+          L.x = (dv & 0xFFFFu) * (L.x >> 12) + slot + (uint32_t)((int32_t)dv >> 16);   // + (-cum)
           ring_renorm(L);
           esc |= sym == 255u;
           sw[e >> 2] += sym << (8 * (e & 3));
@@ -2077,6 +2092,10 @@ static int encode_impl(const skv_params* p, const Paged* pg, const void* d_targe
   uint8_t* ws = static_cast<uint8_t*>(d_workspace);
   CodecArgs a;
   memset(&a, 0, sizeof(a));
+  a.k.k4096 = 4096u;
+  a.k.minus1 = 0xFFFFFFFFu;
+  a.k.k2p20 = 1u << 20;
+  a.k.k8 = 8u;
   a.tgt = static_cast<const uint8_t*>(d_target);
   a.prd = static_cast<const uint8_t*>(d_pred);
   a.tables = static_cast<const uint8_t*>(d_tables);

@@ -140,6 +140,8 @@ def test_table_blob_structures(nat, kind):
             w = int(enc[i, 1])
             sh, h = w & 31, (w >> 7) & 1
             assert w >> 20 == fi and (w >> 8) & 0xFFF == int(c[i]) and (w >> 5) & 3 == 0
+            # s = ceil(log2 fr) and the reciprocal's top bit is 2^32
+            assert h == 1 and (1 << sh) >= fi and (sh == 0 or (1 << (sh - 1)) < fi)
             k = 1 << (32 + sh)
             m = (h << 32) | int(enc[i, 0])
             assert m == -(-k // fi)
@@ -147,7 +149,9 @@ def test_table_blob_structures(nat, kind):
             x1 = fi * (1 << 20) - 1
             assert x1 * (m * fi - k) < k and x1 * m < (1 << 64)
         dec = blob[t, nat.SKV_TABLE_DEC_OFF:nat.SKV_TABLE_DEC_OFF + 1024].copy().view(np.uint32)
-        assert np.array_equal(dec, (f | (c[:256] << 16)).astype(np.uint32))
+        # fr in the lower half, -cum as a signed upper half
+        assert np.array_equal(dec & 0xFFFF, f.astype(np.uint32))
+        assert np.array_equal(dec.view(np.int32) >> 16, -c[:256].astype(np.int32))
         lut = blob[t, nat.SKV_TABLE_LUT_OFF:nat.SKV_TABLE_LUT_OFF + 4096]
         assert np.array_equal(lut, np.repeat(np.arange(256), f).astype(np.uint8))
     if kind == "coef":

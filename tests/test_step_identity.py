@@ -1,14 +1,13 @@
 """Host checks of the integer identity the CUDA encoder step rests on, and of
 the table-layout constants the Python binding mirrors from include/skv.h.
 
-The encoder entry of a symbol with frequency fr holds m = h*2^32 + m_lo =
-ceil(2^(32+s) / fr) for the smallest shift s <= 12 whose rounding error
-keeps floor(x m / 2^(32+s)) equal to floor(x / fr) for every state x below
-the renormalisation threshold fr * 2^20, and the kernel evaluates
-floor(x / fr) as (umulhi(x, m_lo) + h*x) >> s.  The exact condition is
-checked directly at the states that decide it (x = k fr - 1, the largest
-state below each multiple, up to k = 2^20), plus random states, for every
-frequency 1..4095.
+The encoder entry of a symbol with frequency fr holds m = 2^32 + m_lo =
+ceil(2^(32+s) / fr) with s = ceil(log2 fr), which puts m in [2^32, 2^33),
+and the kernel evaluates floor(x / fr) as (umulhi(x, m_lo) + x) >> s for
+every state x below the renormalisation threshold fr * 2^20.  The exact
+condition is checked directly at the states that decide it (x = k fr - 1,
+the largest state below each multiple, up to k = 2^20), plus random states,
+for every frequency 1..4095.
 """
 import random
 import re
@@ -17,18 +16,18 @@ from lossless_kv_cache_fp8_gb300 import native
 
 
 def _entry(fr):
-    for s in range(13):
-        k = 1 << (32 + s)
-        m = -(-k // fr)
-        x1 = fr * (1 << 20) - 1
-        if m < (1 << 33) and x1 * (m * fr - k) < k and x1 * m < (1 << 64):
-            return m, s
-    raise AssertionError(fr)
+    s = (fr - 1).bit_length()           # ceil(log2 fr)
+    k = 1 << (32 + s)
+    m = -(-k // fr)
+    assert (1 << 32) <= m < (1 << 33), fr
+    x1 = fr * (1 << 20) - 1
+    assert x1 * (m * fr - k) < k and x1 * m < (1 << 64), fr
+    return m, s
 
 
 def _kernel_quot(x, m, s):
-    h, m_lo = m >> 32, m & 0xFFFFFFFF
-    t = ((x * m_lo) >> 32) + (x if h else 0)
+    m_lo = m & 0xFFFFFFFF
+    t = ((x * m_lo) >> 32) + x
     assert t < (1 << 32)            # the kernel adds in 32 bits
     return t >> s
 
