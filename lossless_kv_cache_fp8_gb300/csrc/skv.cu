@@ -869,7 +869,8 @@ __device__ unsigned long long chunk_lookback(unsigned long long* st, uint64_t c,
 
 // Warp-cooperative copy of n_w 16-bit words from src to dst (both 2-byte
 // aligned): 32-bit accesses, a 16-bit funnel when the two differ by 2 mod 4,
-// sixteen independent loads in flight per thread (the copy is latency bound).
+// sixteen independent loads in flight per thread (the copy is latency bound);
+// streaming loads and stores (neither side is read again by this kernel).
 __device__ __forceinline__ void warp_copy_words(uint16_t* dst, const uint16_t* src, uint32_t n_w, uint32_t tid) {
   if (n_w == 0) return;
   if ((reinterpret_cast<uintptr_t>(dst) & 3) != 0) {   // make dst 4-byte aligned
@@ -890,7 +891,7 @@ __device__ __forceinline__ void warp_copy_words(uint16_t* dst, const uint16_t* s
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
         const uint32_t k = k0 + u * 32 + tid;
-        if (k < n32) d32[k] = v[u];
+        if (k < n32) __stcs(d32 + k, v[u]);
       }
     }
   } else {
@@ -906,7 +907,7 @@ __device__ __forceinline__ void warp_copy_words(uint16_t* dst, const uint16_t* s
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
         const uint32_t k = k0 + u * 32 + tid;
-        if (k < n32) d32[k] = __funnelshift_r(lo[u], hi[u], 16);
+        if (k < n32) __stcs(d32 + k, __funnelshift_r(lo[u], hi[u], 16));
       }
     }
   }
@@ -1279,7 +1280,7 @@ __global__ void __launch_bounds__(dec_threads(PAGED, MODEL), 1) k_decode_kv(Code
         // raw steps a position consumes at most one word, so the 16 positions
         // read at most 32 bytes: one refill at the group's start keeps the
         // ring ahead of them.
-        const uint32_t x0 = L.x, p0 = L.p, n0 = L.nxt;
+        const uint32_t x0 = L.x, p0 = L.p;
         bool esc = false;
 #pragma unroll
         for (int e = 0; e < G; ++e) {
@@ -1297,7 +1298,7 @@ __global__ void __launch_bounds__(dec_threads(PAGED, MODEL), 1) k_decode_kv(Code
           if (esc) {
             ring_reopen(L, p0);
             L.x = x0;
-            L.nxt = n0;
+            L.nxt = ring_word(L, p0);   // the word at p0, reloaded with the ring
             sw[0] = sw[1] = sw[2] = sw[3] = 0;
 #pragma unroll
             for (int e = 0; e < G; ++e) {
