@@ -156,29 +156,63 @@ def max_over_ranks(v, world, device):
 # ------------------------------------------------------------------------------------------
 # reference arm: the CPU oracle on a bounded sample of the workload
 # ------------------------------------------------------------------------------------------
-def oracle_sample(w, n_slices: int):
-    """first n_slices (layer, kv, head) slices of the workload, generated on the CPU"""
+COEF_SAMPLE_TOKENS = 256   # sample unit of a coefficient stream (a block of whole tokens)
+
+
+def sample_units(w):
+    """sample units of the workload: (layer, kv, head) slices of a KV cache, blocks of
+    COEF_SAMPLE_TOKENS tokens of a coefficient stream"""
     from lossless_kv_cache_fp8_gb300 import synth
+    if w.dtype == synth.COEF:
+        return max(1, w.n_tokens // COEF_SAMPLE_TOKENS)
+    return w.n_layers * w.n_kv * w.n_heads
+
+
+def sample_label(w, n):
+    from lossless_kv_cache_fp8_gb300 import synth
+    if w.dtype == synth.COEF:
+        return f"first {n} of {sample_units(w)} blocks of {COEF_SAMPLE_TOKENS} tokens"
+    return f"first {n} of {sample_units(w)} (layer,kv,head) slices"
+
+
+def oracle_sample(w, n: int):
+    """the first n sample units of the workload, generated on the CPU: a dict with the
+    raw target bits, the prediction (the predictor cache, or the means mu) and, for a
+    coefficient stream, beta and the sample's token count"""
+    from lossless_kv_cache_fp8_gb300 import synth
+    if w.dtype == synth.COEF:
+        q, mu, beta = synth.gen_coef(w, "cpu")
+        rows = min(w.n_tokens, n * COEF_SAMPLE_TOKENS)
+        return {"target": q[:rows].contiguous().reshape(-1).numpy(),
+                "pred": mu[:rows].contiguous().reshape(-1).numpy(), "beta": beta.numpy(), "rows": rows}
     per_layer = w.n_kv * w.n_heads
-    n_layers = (n_slices + per_layer - 1) // per_layer
+    n_layers = (n + per_layer - 1) // per_layer
     t, p = synth.gen_kv(w, "cpu", layers=(0, n_layers))
     sp = w.n_tokens * w.head_dim
-    t = t.reshape(-1)[: n_slices * sp].numpy()
-    p = p.reshape(-1)[: n_slices * sp].numpy()
+    t = t.reshape(-1)[: n * sp].numpy()
+    p = p.reshape(-1)[: n * sp].numpy()
     if w.dtype != synth.FP8:
         t, p = t.view("uint16"), p.view("uint16")
-    return t, p
+    return {"target": t, "pred": p}
 
 
-def run_oracle_round_trip(w, t, p, n_slices):
-    """calibrate + tables + encode + decode of n_slices slices with the oracle; returns seconds"""
+def run_oracle_round_trip(w, s, n):
+    """calibrate + tables + encode + decode of the sample s (n units) with the oracle;
+    returns seconds and the stream's bytes"""
     import numpy as np
     import oracle
+    from lossless_kv_cache_fp8_gb300 import synth
     oracle.build()
-    # n_slices slices as a cache of n_slices heads
-    po = oracle.kv_params(w.dtype, 1, 1, n_slices, w.head_dim, w.n_tokens, w.lane_syms, w.n_calib)
+    t, p = s["target"], s["pred"]
+    if w.dtype == synth.COEF:
+        po = oracle.coef_params(s["rows"], w.n_coef, w.lane_syms)
+    else:   # n slices as a cache of n heads
+        po = oracle.kv_params(w.dtype, 1, 1, n, w.head_dim, w.n_tokens, w.lane_syms, w.n_calib)
     t0 = time.perf_counter()
-    bins, _, _ = oracle.calibrate(po, t, p, want_sum=False)
+    if w.dtype == synth.COEF:
+        bins, _, _ = oracle.calibrate(po, None, s["beta"], want_sum=False)
+    else:
+        bins, _, _ = oracle.calibrate(po, t, p, want_sum=False)
     fr, cum = oracle.build_tables(po)
     st, bs, offs = oracle.encode(po, fr, cum, bins, t, p)
     st2, out = oracle.decode(po, fr, cum, bins, bs, offs, p, t.dtype)
@@ -188,19 +222,19 @@ def run_oracle_round_trip(w, t, p, n_slices):
 
 
 def cpu_baseline(w, target_seconds=12.0):
-    """oracle round trip on the first slices of the workload, about target_seconds of CPU"""
-    t, p = oracle_sample(w, 1)
-    dt1, _ = run_oracle_round_trip(w, t, p, 1)
-    n = max(1, min(w.n_layers * w.n_kv * w.n_heads, int(target_seconds / max(dt1, 1e-3))))
+    """oracle round trip on the first units of the workload, about target_seconds of CPU"""
+    s = oracle_sample(w, 1)
+    dt1, _ = run_oracle_round_trip(w, s, 1)
+    n = max(1, min(sample_units(w), int(target_seconds / max(dt1, 1e-3))))
     if n > 1:
-        t, p = oracle_sample(w, n)
-        dt, _ = run_oracle_round_trip(w, t, p, n)
+        s = oracle_sample(w, n)
+        dt, _ = run_oracle_round_trip(w, s, n)
     else:
         dt = dt1
-    raw = t.nbytes
+    raw = s["target"].nbytes
     return {"value": raw / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {n} of {w.n_layers * w.n_kv * w.n_heads} (layer,kv,head) slices "
-                      f"({raw / 1e6:.1f} MB raw KV), single-threaded calibrate+tables+encode+decode"}
+            "sample": f"{sample_label(w, n)} ({raw / 1e6:.1f} MB raw), "
+                      f"single-threaded calibrate+tables+encode+decode"}
 
 
 def main_reference(args):
@@ -209,24 +243,24 @@ def main_reference(args):
     if rank != 0:
         return
     w = synth.WORKLOADS[args.workload]
-    n_slices = max(1, args.ref_slices)
-    t, p = oracle_sample(w, n_slices)
+    n = max(1, min(args.ref_slices, sample_units(w)))
+    s = oracle_sample(w, n)
     for _ in range(args.warmup):
-        run_oracle_round_trip(w, t, p, n_slices)
+        run_oracle_round_trip(w, s, n)
     times = []
     for _ in range(args.steps):
-        dt, _ = run_oracle_round_trip(w, t, p, n_slices)
+        dt, _ = run_oracle_round_trip(w, s, n)
         times.append(dt)
     total = sum(times)
-    raw = t.nbytes
+    raw = s["target"].nbytes
     v = raw * len(times) / total / 1e9
-    sample = (f"first {n_slices} of {w.n_layers * w.n_kv * w.n_heads} (layer,kv,head) slices "
-              f"({raw / 1e6:.1f} MB raw KV) per step, single-threaded")
+    sample = f"{sample_label(w, n)} ({raw / 1e6:.1f} MB raw) per step, single-threaded"
+    dtype = {synth.FP8: "u8", synth.BF16: "u16", synth.COEF: "i16"}[w.dtype]
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "u8" if w.dtype == synth.FP8 else "u16", "data": "synthetic",
+        "dtype": dtype, "data": "synthetic",
         "config": {"workload": w.name, "sample": sample},
         "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -563,7 +597,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--ref-slices", type=int, default=2, help="reference arm: slices per step")
+    ap.add_argument("--ref-slices", type=int, default=2,
+                    help="reference arm: sample units per step ((layer,kv,head) slices of a KV cache, "
+                         "blocks of 256 tokens of a coefficient stream)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -16,10 +16,10 @@ def _lines(out):
     return [json.loads(l) for l in out.splitlines() if l.startswith("{")]
 
 
-def _check(line, n):
+def _check(line, n, workload="qwen3-32b-128k-fp8"):
     assert KEYS <= set(line), KEYS - set(line)
     assert line["impl"] == "reference" and line["n_gpus"] == n and line["value"] > 0
-    assert line["config"]["workload"] == "qwen3-32b-128k-fp8"
+    assert line["config"]["workload"] == workload
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
     e = line["e2e"]
@@ -34,6 +34,18 @@ def test_reference_arm_one_process():
     lines = _lines(r.stdout)
     assert len(lines) == 1
     _check(lines[0], 1)
+
+
+def test_reference_arm_coefficient_stream():
+    # a coefficient stream's sample unit is a block of whole tokens
+    w = "hybrid-coef-32k-x2048"
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", w, "--steps", "1",
+                        "--warmup", "0", "--ref-slices", "1"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = _lines(r.stdout)
+    assert len(lines) == 1
+    _check(lines[0], 1, w)
+    assert lines[0]["dtype"] == "i16" and "blocks of 256 tokens" in lines[0]["config"]["sample"]
 
 
 def test_reference_arm_two_ranks():
