@@ -1387,23 +1387,46 @@ __device__ __forceinline__ void coef_load(const CodecArgs& a, uint64_t p0, uint3
   R.m1 = make_float4(mv[4], mv[5], mv[6], mv[7]);
   R.q = make_uint4(qw[0], qw[1], qw[2], qw[3]);
 }
-__device__ __forceinline__ void coef_group(const CodecArgs& a, uint64_t p0, uint32_t ne, const CoefRaw& R,
+// c = the component of the group's first position (callers step it from
+// group to group: no 64-bit remainder per group).  A whole group whose
+// components do not wrap reads its 8 bins as one 8-byte vector.
+__device__ __forceinline__ void coef_group(const CodecArgs& a, uint32_t c, uint32_t ne, const CoefRaw& R,
                                            CoefGroup& G) {
   const float mv[8] = {R.m0.x, R.m0.y, R.m0.z, R.m0.w, R.m1.x, R.m1.y, R.m1.z, R.m1.w};
   const uint32_t qw[4] = {R.q.x, R.q.y, R.q.z, R.q.w};
-  uint32_t c = (uint32_t)(p0 % a.C);
+  uint32_t bins[8];
+  if (ne == 8 && c + 8 <= a.C && (c & 7u) == 0) {
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(a.bins + c));
+#pragma unroll
+    for (int e = 0; e < 8; ++e) bins[e] = ((e < 4 ? v.x : v.y) >> (8 * (e & 3))) & 0xFFu;
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      bins[e] = (uint32_t)e < ne ? __ldg(a.bins + c) : 0xFFu;
+      c = c + 1 == a.C ? 0 : c + 1;
+    }
+  }
   G.skip = 0;
+  bool bad = false;
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     G.q[e] = (int16_t)(qw[e >> 1] >> (16 * (e & 1)));
-    const uint32_t bin = (uint32_t)e < ne ? __ldg(a.bins + c) : 0xFFu;
-    c = c + 1 == a.C ? 0 : c + 1;
     uint32_t f;
     coef_mean(mv[e], &G.m[e], &f);
-    G.tbl[e] = 16u * bin + f;
-    if (bin == 0xFFu) G.skip |= 1u << e;
-    else if (bin > 63u) { atomicOr(a.status, SKV_FLAG_BAD_BIN); G.tbl[e] = 1023; }
+    const uint32_t bin = bins[e];
+    G.skip |= (bin == 0xFFu ? 1u : 0u) << e;
+    bad |= bin > 63u && bin != 0xFFu;
+    G.tbl[e] = 16u * min(bin, 63u) + f;   // a skipped component's table is never read
   }
+  if (bad) atomicOr(a.status, SKV_FLAG_BAD_BIN);
+}
+// component of the previous / next group of a lane (groups 256 positions apart)
+__device__ __forceinline__ uint32_t coef_comp_back(uint32_t c, uint32_t step, uint32_t C) {
+  return c >= step ? c - step : c + C - step;
+}
+__device__ __forceinline__ uint32_t coef_comp_fwd(uint32_t c, uint32_t step, uint32_t C) {
+  const uint32_t n = c + step;
+  return n >= C ? n - C : n;
 }
 
 // One coding step where do_it holds; elsewhere x and the stream are left alone
@@ -1443,6 +1466,8 @@ __global__ void __launch_bounds__(256) k_encode_coef(CodecArgs a) {
     auto gpos = [&](int i) { return first + ((uint64_t)i * 32 + lane) * 8; };   // position of group i
     auto gnum = [&](uint64_t p0) { return (uint32_t)min((uint64_t)8, first + n_pos - p0); };
     CoefRaw R;
+    const uint32_t step = 256u % a.C;
+    uint32_t comp = n_g ? (uint32_t)(gpos((int)n_g - 1) % a.C) : 0u;   // component of the lane's current group
     if (n_g) coef_load(a, gpos((int)n_g - 1), gnum(gpos((int)n_g - 1)), true, R);
     for (int i = n_iter - 1; i >= 0; --i) {
       const uint32_t act = __ballot_sync(0xFFFFFFFFu, i < (int)n_g);
@@ -1450,7 +1475,8 @@ __global__ void __launch_bounds__(256) k_encode_coef(CodecArgs a) {
       const uint64_t p0 = gpos(i);
       const uint32_t ne = gnum(p0);
       CoefGroup G;
-      coef_group(a, p0, ne, R, G);
+      coef_group(a, comp, ne, R, G);
+      comp = coef_comp_back(comp, step, a.C);
       if (i > 0) coef_load(a, gpos(i - 1), gnum(gpos(i - 1)), true, R);
       uint2 en[8];
       uint32_t esc = 0;
@@ -1508,6 +1534,8 @@ __global__ void __launch_bounds__(256) k_decode_coef(CodecArgs a) {
     auto gpos = [&](uint32_t i) { return first + ((uint64_t)i * 32 + lane) * 8; };
     auto gnum = [&](uint64_t p0) { return (uint32_t)min((uint64_t)8, first + n_pos - p0); };
     CoefRaw R;
+    const uint32_t step = 256u % a.C;
+    uint32_t comp = n_g ? (uint32_t)(gpos(0) % a.C) : 0u;   // component of the lane's current group
     if (n_g) coef_load(a, gpos(0), gnum(gpos(0)), false, R);
     for (uint32_t i = 0; i < n_iter; ++i) {
       const uint32_t act = __ballot_sync(0xFFFFFFFFu, i < n_g);
@@ -1515,7 +1543,8 @@ __global__ void __launch_bounds__(256) k_decode_coef(CodecArgs a) {
       const uint64_t p0 = gpos(i);
       const uint32_t ne = gnum(p0);
       CoefGroup G;
-      coef_group(a, p0, ne, R, G);
+      coef_group(a, comp, ne, R, G);
+      comp = coef_comp_fwd(comp, step, a.C);
       if (i + 1 < n_g) coef_load(a, gpos(i + 1), gnum(gpos(i + 1)), false, R);
       uint32_t qo[4] = {0, 0, 0, 0};
 #pragma unroll
