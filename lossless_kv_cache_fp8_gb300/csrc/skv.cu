@@ -1512,7 +1512,9 @@ __global__ void __launch_bounds__(256) k_encode_coef(CodecArgs a) {
 }
 
 // Decoding reads one slot entry per step (symbol, frequency and offset: see
-// the table layout), a dependent L2 read: the step chain is bound by its latency.
+// the table layout), a dependent L2 read: the step chain is bound by its latency,
+// so nothing else sits between two reads of a lane (escapes are handled by
+// redoing the group).
 __global__ void __launch_bounds__(256) k_decode_coef(CodecArgs a) {
   const uint32_t lane = threadIdx.x & 31;
   const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
@@ -1546,7 +1548,12 @@ __global__ void __launch_bounds__(256) k_decode_coef(CodecArgs a) {
       coef_group(a, comp, ne, R, G);
       comp = coef_comp_fwd(comp, step, a.C);
       if (i + 1 < n_g) coef_load(a, gpos(i + 1), gnum(gpos(i + 1)), false, R);
+      // The group is decoded assuming no escape (no vote between the dependent
+      // table reads); lanes that met one decode it again from the saved state
+      // with the raw steps.
       uint32_t qo[4] = {0, 0, 0, 0};
+      const uint32_t x0 = L.x, p0w = L.p, n0 = L.nxt;
+      bool esc = false;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const bool d = !((G.skip >> e) & 1u);
@@ -1555,14 +1562,35 @@ __global__ void __launch_bounds__(256) k_decode_coef(CodecArgs a) {
         const uint32_t xn = ((se >> 8) & 0xFFFu) * (L.x >> 12) + (se >> 20);
         L.x = d ? xn : L.x;
         dec_renorm(L);                    // a skipped position leaves x >= 2^16: no renormalisation
-        uint32_t r = (uint32_t)((int)sym - 127);
-        if (__any_sync(act, d && sym == 255u)) {
-          if (d && sym == 255u) {
-            r = dec_raw(L);
-            r = (r << 8) | dec_raw(L);
+        esc |= d && sym == 255u;
+        qo[e >> 1] |= (d ? (((uint32_t)G.m[e] + sym - 127u) & 0xFFFFu) : 0u) << (16 * (e & 1));
+      }
+      const uint32_t redo = __ballot_sync(act, esc);
+      if (redo) {
+        if (esc) {
+          L.x = x0;
+          L.p = p0w;
+          L.nxt = n0;
+          qo[0] = qo[1] = qo[2] = qo[3] = 0;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const bool d = !((G.skip >> e) & 1u);
+            const uint32_t se = __ldg(slot_tab + (d ? G.tbl[e] : 0u) * 4096u + (L.x & 4095u));
+            const uint32_t sym = se & 0xFFu;
+            const uint32_t xn = ((se >> 8) & 0xFFFu) * (L.x >> 12) + (se >> 20);
+            L.x = d ? xn : L.x;
+            dec_renorm(L);
+            uint32_t r = (uint32_t)((int)sym - 127);
+            if (__any_sync(redo, d && sym == 255u)) {
+              if (d && sym == 255u) {
+                r = dec_raw(L);
+                r = (r << 8) | dec_raw(L);
+              }
+            }
+            qo[e >> 1] |= (d ? (((uint32_t)G.m[e] + r) & 0xFFFFu) : 0u) << (16 * (e & 1));
           }
         }
-        qo[e >> 1] |= (d ? (((uint32_t)G.m[e] + r) & 0xFFFFu) : 0u) << (16 * (e & 1));
+        __syncwarp(act);
       }
       if (ne == 8) {
         *reinterpret_cast<uint4*>(q + p0) = make_uint4(qo[0], qo[1], qo[2], qo[3]);
