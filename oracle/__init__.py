@@ -60,7 +60,9 @@ _lib = None
 def lib():
     global _lib
     if _lib is None:
-        _lib = C.CDLL(build())
+        # SKV_ORACLE_LIB: a different build of the same source (the mutation
+        # check of tests/oracle_mutations.py loads copies with planted mistakes)
+        _lib = C.CDLL(os.environ.get("SKV_ORACLE_LIB") or build())
         P = C.POINTER(Params)
         vp = C.c_void_p
         u64, u32, i32 = C.c_uint64, C.c_uint32, C.c_int
