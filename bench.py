@@ -282,6 +282,8 @@ def main_ours(args):
     w = synth.WORKLOADS[args.workload]
     if args.layers:
         w = w.scaled(n_layers=args.layers)
+    if args.lane_syms:
+        w = w.scaled(lane_syms=args.lane_syms)
     p = native.params_for(w, model=args.model)
     sz = native.sizes(p)
     stream = torch.cuda.current_stream(dev)
@@ -399,18 +401,20 @@ def main_ours(args):
 
 
 def e2e(args, w, codec, tgt, prd, cal, out, stream, dev, total):
-    """The same step through the C ABI with the inputs in pinned host memory and the
-    stream read back.  KV caches go through pipeline.HostPipeline (layer groups:
-    host->device copies, coding and the device->host copy of the stream overlap on
-    three streams; the joined stream is checked byte for byte against the one-call
-    stream); coefficient streams are copied in, coded and copied back in sequence."""
-    import numpy as np
+    """The same round trip through the C ABI from host buffers.  KV caches:
+    skv_encode_host (pinned target + prediction in, stream + lane offsets out)
+    then skv_decode_host (stream + offsets + prediction in, decoded target out),
+    each coding layer groups with the copies overlapped on three streams inside
+    the library; the stream, offsets and decoded cache are checked against the
+    one-call results.  Coefficient streams are copied in, coded and copied back
+    in sequence."""
     import torch
     from lossless_kv_cache_fp8_gb300 import native, pipeline, synth
     try:
         h_t = torch.empty(tgt.shape, dtype=tgt.dtype, pin_memory=True)
         h_p = torch.empty(prd.shape, dtype=prd.dtype, pin_memory=True)
         h_bs = torch.empty(int(total * 1.05) + 4096, dtype=torch.uint8, pin_memory=True)
+        h_out = torch.empty(tgt.shape, dtype=tgt.dtype, pin_memory=True) if w.dtype != synth.COEF else None
     except RuntimeError as e:
         return {"value": None, "unit": "GB/s", "error": f"pinned host allocation failed: {e}"[:200]}
     h_t.copy_(tgt)
@@ -423,15 +427,15 @@ def e2e(args, w, codec, tgt, prd, cal, out, stream, dev, total):
         groups = max(1, min(16, w.n_layers))
         pipe = pipeline.HostPipeline(codec.p, group_layers=-(-w.n_layers // groups), device=dev,
                                      cap_frac=args.cap_frac)
-    out.zero_()   # every step must write the whole decoded cache again
-    times = []
+    times, t_enc, t_dec = [], [], []
     nb = 0
     for k in range(args.warmup + max(1, args.e2e_steps)):
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
         if kv:
-            n = pipe.run(h_t, h_p, h_bs, h_off, decode_into=out, stream=stream)
+            n = pipe.encode(h_t, h_p, h_bs, h_off)
+            t1 = time.perf_counter()
+            pipe.decode(h_bs, n, h_off, h_p, h_out)
         else:
             tgt.copy_(h_t, non_blocking=True)
             prd.copy_(h_p, non_blocking=True)
@@ -440,25 +444,34 @@ def e2e(args, w, codec, tgt, prd, cal, out, stream, dev, total):
             n = codec.encode(tgt, prd, want_total=True)
             h_bs[:n].copy_(codec.bitstream[:n], non_blocking=True)
             h_off.copy_(codec.lane_offsets, non_blocking=True)
+            torch.cuda.synchronize()
+            t1 = time.perf_counter()
             codec.decode(prd, out, n_bytes=n)
-        t1.record(stream)
         torch.cuda.synchronize()
+        t2 = time.perf_counter()
         if k >= args.warmup:
-            times.append(t0.elapsed_time(t1))
+            times.append((t2 - t0) * 1e3)
+            t_enc.append((t1 - t0) * 1e3)
+            t_dec.append((t2 - t1) * 1e3)
         nb = n
-    assert torch.equal(out, tgt)
     res = {}
     if kv:
-        assert pipe.check() == native.SKV_OK
         assert nb == total and torch.equal(h_bs[:nb], codec.bitstream[:nb].cpu())
-        assert np.array_equal(pipe.joined_offsets(h_off.numpy()), codec.lane_offsets.cpu().numpy().view(np.uint64))
-        res["pipeline"] = {"layer_groups": len(pipe.groups), "streams": 3,
-                           "check": "joined stream and offsets equal the one-call stream"}
+        assert torch.equal(h_off, codec.lane_offsets.cpu())
+        assert torch.equal(h_out, tgt.cpu())
+        res["pipeline"] = {"layer_groups": len(pipe.groups), "streams": 3, "calls": "skv_encode_host, skv_decode_host",
+                           "check": "stream, offsets and decoded cache equal the one-call results"}
+        h2d = 2 * w.raw_bytes + nb + h_off.numel() * 8 + w.raw_bytes   # encode: target + prediction; decode: stream + offsets + prediction
+        d2h = nb + h_off.numel() * 8 + w.raw_bytes                       # encode: stream + offsets; decode: target
+    else:
+        assert torch.equal(out, tgt)
+        h2d = h_t.numel() * h_t.element_size() + h_p.numel() * h_p.element_size()
+        d2h = nb + h_off.numel() * 8
     ms = statistics.mean(times)
-    h2d = h_t.numel() * h_t.element_size() + h_p.numel() * h_p.element_size()
-    d2h = nb + h_off.numel() * 8
     return {"value": w.raw_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": len(times), **res}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "encode_ms": statistics.mean(t_enc),
+            "decode_ms": statistics.mean(t_dec), "steps": len(times),
+            "timing": "host wall clock around the synchronous calls (copies included)", **res}
 
 
 def paged_run(args, w, codec, tgt, prd, stream, total, peak):
@@ -587,6 +600,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling cases)")
+    ap.add_argument("--lane-syms", type=int, default=0, help="override the positions per lane of the workload")
     ap.add_argument("--cap-frac", type=float, default=0.6, help="bitstream buffer / raw bytes")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--paged", type=int, default=0, help="also time paged pools with this many tokens per block")

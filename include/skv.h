@@ -200,7 +200,9 @@ int skv_encode(const skv_params* p, const void* d_target, const void* d_pred,
  * d_target_out (COEF: q int16; switched-off components are 0).  A lane whose
  * stream does not end in the initial state or does not consume exactly its
  * words, or offsets that are not increasing and inside n_bytes, set
- * SKV_FLAG_CORRUPT in d_status (cleared by the call first). */
+ * SKV_FLAG_CORRUPT in d_status (cleared by the call first).  The decoder reads
+ * the stream in aligned 16-byte blocks: d_bitstream must be readable up to
+ * n_bytes rounded up to a multiple of 16 (the bytes past n_bytes are ignored). */
 int skv_decode(const skv_params* p, const void* d_bitstream, uint64_t n_bytes,
                const uint64_t* d_lane_offsets, const void* d_pred, const void* d_tables,
                const uint8_t* d_bins, void* d_target_out, uint32_t* d_status, void* stream);
@@ -276,7 +278,8 @@ int skv_decode_paged(const skv_params* p, const skv_paged_layout* layout, const 
  * (x and g as bf16 matrices and bf16 copies of V and U).
  * d_status: one caller-owned device word, cleared by the call; a kernel that
  * waited over about a second on its own pipeline sets SKV_FLAG_TIMEOUT
- * (read it with skv_read_status).  Argument errors return
+ * (read it with skv_read_status); its output tile is then not written
+ * (d_mu_out is undefined after a timeout).  Argument errors return
  * SKV_ERR_INVALID_ARG and launch nothing; SKV_ERR_UNSUPPORTED if the driver
  * offers no tensor-map encoder. */
 typedef struct {
@@ -290,6 +293,51 @@ int skv_ctx_means(const skv_ctx_map* map, const int16_t* d_q_even, uint64_t n_ev
                   uint64_t n_odd, uint32_t n_coef, float* d_mu_out, void* d_scratch, uint64_t scratch_bytes,
                   uint32_t* d_status, void* stream);
 
+/* Host-resident caches ([SKV] core idea: the coded cache is what moves between
+ * machines or sits in a prefix store; [VeriCache] "operational
+ * considerations": a full KV cache that lives in host memory crosses the host
+ * link, so the codec runs alongside the copies).  The target and prediction
+ * caches (and, for decoding, the stream and its lane offsets) are in host
+ * memory; page-locked memory (cudaHostAlloc / cudaMallocHost) lets the copies
+ * overlap the kernels, pageable memory works but serialises them.  KV dtypes
+ * only (COEF: SKV_ERR_UNSUPPORTED).
+ *
+ * The cache is coded in groups of group_layers layers (a layer range is an
+ * independent sub-cache: chunks never straddle a slice, calibration is per
+ * channel, tables depend only on the dtype), double-buffered in d_workspace
+ * (skv_host_workspace_bytes(p, group_layers, group_cap_bytes) bytes, 16-byte
+ * aligned, caller-owned): while group k is calibrated and coded on streams[1],
+ * group k + 1 is copied in on streams[0] and group k - 1 copied out on
+ * streams[2] (three caller-owned cudaStream_t).  group_cap_bytes bounds one
+ * group's stream on the device (0: the group's worst case); a group that needs
+ * more fails with SKV_ERR_CAPACITY.  Both calls are synchronous: they return
+ * when every copy has landed, with the most serious status of any group (the
+ * kernels' flags included).  They create and destroy a few CUDA events but
+ * allocate no memory.
+ *
+ * skv_encode_host: calibrates every group into d_bins (n_channels, device,
+ * written in full), encodes it with d_tables (from skv_build_tables) and writes
+ * the stream to h_bitstream (cap_bytes) and the whole-cache lane offsets to
+ * h_lane_offsets[n_lanes + 1]: the result is byte-identical to skv_calibrate +
+ * skv_encode of the whole cache on the device.  *h_total_bytes (if non-NULL)
+ * receives the stream size.  The device computes each group's place in the
+ * stream; the host reads it from the offsets copied back, one group behind,
+ * so the coding stream never waits on the host.
+ *
+ * skv_decode_host: decodes the stream (h_bitstream, n_bytes, h_lane_offsets)
+ * against the prediction h_pred with d_tables and d_bins into h_target_out
+ * (the cache's size).  Offsets that are not increasing or not inside n_bytes
+ * give SKV_ERR_CORRUPT before anything is launched. */
+uint64_t skv_host_workspace_bytes(const skv_params* p, uint32_t group_layers, uint64_t group_cap_bytes);
+int skv_encode_host(const skv_params* p, const void* h_target, const void* h_pred, const void* d_tables,
+                    uint8_t* d_bins, void* h_bitstream, uint64_t cap_bytes, uint64_t* h_lane_offsets,
+                    uint64_t* h_total_bytes, uint32_t group_layers, uint64_t group_cap_bytes, void* d_workspace,
+                    uint64_t workspace_bytes, void* const* streams);
+int skv_decode_host(const skv_params* p, const void* h_bitstream, uint64_t n_bytes, const uint64_t* h_lane_offsets,
+                    const void* h_pred, const void* d_tables, const uint8_t* d_bins, void* h_target_out,
+                    uint32_t group_layers, uint64_t group_cap_bytes, void* d_workspace, uint64_t workspace_bytes,
+                    void* const* streams);
+
 /* Encode without a caller-provided workspace.  The pages have no counterpart
  * to this call; it exists for callers that cannot allocate device memory, such
  * as code handed only its input and output buffers by a host framework that
@@ -299,17 +347,19 @@ int skv_ctx_means(const skv_ctx_map* map, const int16_t* d_q_even, uint64_t n_ev
  * Same arguments and results as skv_encode minus the workspace.  The scratch
  * is a file-scope device array of SKV_NOALLOC_SCRATCH_BYTES (64 MiB) inside
  * libskv.so, which every GPU that loads the library holds until the process
- * exits.  Streams whose skv_encode_workspace_bytes exceeds that size are
- * rejected with SKV_ERR_UNSUPPORTED before anything is launched (for FP8 with
- * lane_syms 1024 the limit is about 16 million positions).
+ * exits.  A stream fits when skv_encode_workspace_bytes(p) is at most that
+ * size: about 8.3 million FP8 positions (254 chunks at lane_syms 1024, 63 at
+ * 4096) or 5.5 million BF16 positions (170 chunks at lane_syms 1024); larger
+ * streams are rejected with SKV_ERR_UNSUPPORTED before anything is launched.
  *
  * The first call on a device looks up the array's device address on the
  * current device (once per device, then cached); make that first call before
  * any stream capture.  The call itself allocates nothing and frees nothing.
  * Every call on a device shares the one array and it keeps the last call's
- * contents; nothing in it needs clearing, because the encoder writes every
- * scratch word before reading it.  Calls whose work overlaps on the GPU
- * (different streams, or other host threads) race on the array: serialise them. */
+ * contents: the call clears the per-chunk look-back states and the chunk
+ * ticket itself, and every other scratch word is written before it is read.
+ * Calls whose work overlaps on the GPU (different streams, or other host
+ * threads) race on the array: serialise them. */
 #define SKV_NOALLOC_SCRATCH_BYTES (64ull << 20)
 int skv_encode_noalloc(const skv_params* p, const void* d_target, const void* d_pred,
                        const void* d_tables, const uint8_t* d_bins, void* d_bitstream,
@@ -334,6 +384,18 @@ int skv_selftest_lookback(uint64_t* d_state, uint32_t n_chunks, uint32_t missing
  * free its tensor memory and return.  d_scratch: 48 KB, 16-byte aligned,
  * caller-owned (its contents are overwritten). */
 int skv_selftest_ctx_wait(void* d_scratch, uint32_t* d_status, void* stream);
+
+/* Checked build (no counterpart on the pages; it stands in for a memory
+ * checker): a library compiled with -DSKV_CHECKED=1 checks every
+ * shared-memory access of the codec kernels against the launch's shared size
+ * and alignment, and the encoder's table, word-buffer and scratch-slot
+ * cursors, the decoder's output rows, the chunk copy into the stream and the
+ * coefficient table indices against their own regions.  A failed check is
+ * counted, the first failing site is kept and the access is skipped; nothing
+ * traps.  This call synchronises the device, returns the count and the first
+ * site in *h_count / *h_first_site and clears both.  In the ordinary build it
+ * returns SKV_ERR_UNSUPPORTED. */
+int skv_checked_failures(uint32_t* h_count, uint32_t* h_first_site);
 
 /* Synchronises the stream, reads the status word and returns SKV_OK or the
  * code of the most serious flag (CORRUPT > CAPACITY > TIMEOUT > INVALID_ARG

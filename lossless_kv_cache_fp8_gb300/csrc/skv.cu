@@ -257,19 +257,74 @@ __device__ __forceinline__ void model_exp_tables(const uint32_t* bw, const uint4
   for (int k = 0; k < 4; ++k) model_exp_word(bw[k], word_of(praw, k), stride, tb + 4 * k);
 }
 
+// ---- checked build -----------------------------------------------------------
+// With -DSKV_CHECKED=1 every shared-memory access of the codec kernels is
+// checked against the launch's dynamic shared size and its natural alignment,
+// and the encoder's table, word-buffer and scratch-slot cursors, the decoder's
+// output rows, the chunk copy into the stream and the coefficient kernels'
+// table indices against their own regions.  A failed check counts itself,
+// records the first failing site and skips the access (a read gives 0); it
+// never traps.  skv_checked_failures reads and clears the record.
+#ifndef SKV_CHECKED
+#define SKV_CHECKED 0
+#endif
+#if SKV_CHECKED
+__device__ unsigned int g_check_count;
+__device__ unsigned int g_check_site;
+__device__ __noinline__ void check_fail(uint32_t site) {
+  atomicAdd(&g_check_count, 1u);
+  atomicCAS(&g_check_site, 0u, site);
+}
+__device__ __forceinline__ uint32_t dyn_smem_bytes() {
+  uint32_t v;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(v));
+  return v;
+}
+__device__ __forceinline__ bool smem_ok(uint32_t a, uint32_t n, uint32_t site) {
+  const bool ok = (uint64_t)a + n <= dyn_smem_bytes() && (a & (n - 1)) == 0;
+  if (!ok) check_fail(site);
+  return ok;
+}
+#define SKV_CHECK(cond, site)        \
+  do {                               \
+    if (!(cond)) check_fail(site);   \
+  } while (0)
+#define SKV_SMEM_OK(a, n, site) smem_ok(a, n, site)
+#else
+#define SKV_CHECK(cond, site) \
+  do {                        \
+  } while (0)
+#define SKV_SMEM_OK(a, n, site) true
+#endif
+// check sites (the value recorded for the first failure)
+enum : uint32_t {
+  kSiteSmemLoad = 1, kSiteSmemStore = 2, kSiteEncEntry = 3, kSiteWordBuffer = 4, kSiteScratchSlot = 5,
+  kSiteStreamCopy = 6, kSiteDecOut = 7, kSiteRing = 8, kSiteCoefTable = 9
+};
+
 // ---- shared-memory access by byte offset into the dynamic shared array -----
 // Plain C++ accesses (not volatile asm) so that the compiler may predicate and
 // schedule them like any other instruction.
 extern __shared__ __align__(16) uint8_t g_smem[];
 __device__ __forceinline__ void sts_u16(uint32_t a, uint32_t v) {
-  *reinterpret_cast<uint16_t*>(g_smem + a) = (uint16_t)v;
+  if (SKV_SMEM_OK(a, 2, kSiteSmemStore)) *reinterpret_cast<uint16_t*>(g_smem + a) = (uint16_t)v;
 }
-__device__ __forceinline__ uint32_t lds_u16(uint32_t a) { return *reinterpret_cast<const uint16_t*>(g_smem + a); }
-__device__ __forceinline__ uint32_t lds_u8(uint32_t a) { return g_smem[a]; }
-__device__ __forceinline__ uint32_t lds_u32(uint32_t a) { return *reinterpret_cast<const uint32_t*>(g_smem + a); }
-__device__ __forceinline__ uint2 lds_u64(uint32_t a) { return *reinterpret_cast<const uint2*>(g_smem + a); }
-__device__ __forceinline__ uint4 lds_u128(uint32_t a) { return *reinterpret_cast<const uint4*>(g_smem + a); }
-__device__ __forceinline__ void sts_u128(uint32_t a, uint4 v) { *reinterpret_cast<uint4*>(g_smem + a) = v; }
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
+  return SKV_SMEM_OK(a, 2, kSiteSmemLoad) ? *reinterpret_cast<const uint16_t*>(g_smem + a) : 0u;
+}
+__device__ __forceinline__ uint32_t lds_u8(uint32_t a) { return SKV_SMEM_OK(a, 1, kSiteSmemLoad) ? g_smem[a] : 0u; }
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+  return SKV_SMEM_OK(a, 4, kSiteSmemLoad) ? *reinterpret_cast<const uint32_t*>(g_smem + a) : 0u;
+}
+__device__ __forceinline__ uint2 lds_u64(uint32_t a) {
+  return SKV_SMEM_OK(a, 8, kSiteSmemLoad) ? *reinterpret_cast<const uint2*>(g_smem + a) : make_uint2(0, 0);
+}
+__device__ __forceinline__ uint4 lds_u128(uint32_t a) {
+  return SKV_SMEM_OK(a, 16, kSiteSmemLoad) ? *reinterpret_cast<const uint4*>(g_smem + a) : make_uint4(0, 0, 0, 0);
+}
+__device__ __forceinline__ void sts_u128(uint32_t a, uint4 v) {
+  if (SKV_SMEM_OK(a, 16, kSiteSmemStore)) *reinterpret_cast<uint4*>(g_smem + a) = v;
+}
 __device__ __forceinline__ void stg_u128(void* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 
 // Encoder entry {m_lo, w}, w = fr << 20 | cum << 8 | 1 << 7 | s with
@@ -391,6 +446,7 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // block rb -> ring slot rb mod 4 (zero bytes read past the lane's last block)
 __device__ __forceinline__ void ring_step(RingLane& L) {
   const uint32_t saddr = (uint32_t)__cvta_generic_to_shared(g_smem + L.ring + (L.rb & 3u) * 16u);
+  if (!SKV_SMEM_OK(L.ring + (L.rb & 3u) * 16u, 16, kSiteRing)) return;
   const bool valid = L.rb <= L.last;
   const uint8_t* src = L.base + (valid ? ((uint64_t)L.rb << 4) : 0);
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr), "l"(src), "r"(valid ? 16u : 0u)
@@ -825,6 +881,10 @@ __device__ __forceinline__ void chunk_publish(unsigned long long* st, uint64_t c
 // (whole warp calls): walks back over the predecessors 32 at a time, adding
 // aggregates until an inclusive prefix, waiting (bounded) on any that is
 // still coding; then publishes c's inclusive prefix.  ~0 if it failed.
+// The batch where the walk stops also gets its walked chunks' inclusive
+// prefixes published (each one is the found prefix plus the aggregates below
+// it in the batch, the value any later walk would compute), so that walks
+// from later chunks stop sooner.
 __device__ unsigned long long chunk_resolve(unsigned long long* st, uint64_t c, unsigned long long total,
                                             uint32_t* status, uint32_t max_spins) {
   const uint32_t tid = threadIdx.x & 31;
@@ -848,8 +908,20 @@ __device__ unsigned long long chunk_resolve(unsigned long long* st, uint64_t c, 
     if (stop && ((v >> 62) == 3) && tid == (uint32_t)(__ffs(stop) - 1)) failed = true;
     failed = __any_sync(0xFFFFFFFFu, failed);
     if (failed) break;
-    excl += warp_sum64(((upto >> tid) & 1) ? (v & kStVal) : 0ull);
-    if (stop) break;
+    const unsigned long long mine = ((upto >> tid) & 1) ? (v & kStVal) : 0ull;
+    if (stop) {
+      // suffix sums over lanes tid..first stop: the inclusive prefix of chunk j - tid
+      unsigned long long suf = mine;
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long u = __shfl_down_sync(0xFFFFFFFFu, suf, o);
+        if (tid + o < 32) suf += u;
+      }
+      const uint32_t s0 = (uint32_t)(__ffs(stop) - 1);
+      if (tid < s0 && idx >= 0) st_release(&st[idx], kStInc | suf);
+      excl += __shfl_sync(0xFFFFFFFFu, suf, 0);
+      break;
+    }
+    excl += warp_sum64(mine);
     j -= 32;
   }
   if (failed) {
@@ -938,6 +1010,7 @@ __device__ __noinline__ void place_chunk(const CodecArgs& a, unsigned long long 
     const uint32_t n_w = __shfl_sync(0xFFFFFFFFu, len, l) >> 1;
     const unsigned long long dst = __shfl_sync(0xFFFFFFFFu, lane_off, l);
     const uint32_t owner = (l % CS) * R + l / CS;
+    SKV_CHECK(dst + 2ull * n_w <= a.cap && 2ull * n_w <= 2 * a.slot_words, kSiteStreamCopy);
     const uint16_t* src = reinterpret_cast<const uint16_t*>(
         reinterpret_cast<const uint8_t*>(a.slots + (sset * kLanes + owner + 1) * a.slot_words)) - n_w;
     warp_copy_words(reinterpret_cast<uint16_t*>(a.out_bs + dst), src, n_w, tid);
@@ -1120,11 +1193,15 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
           // byte offset of the entry: 8 * symbol (the upper lane's shift
           // also drops the lower lane, whose value is below 2^13)
           const uint32_t tbe = MODEL ? t4[e & 3] : tb[e];
+          uint32_t ad;
           if (ESZ == 1) {
             const uint32_t v = (e & 1) ? vo[e >> 2] : ve[e >> 2];
-            return (e & 2) ? tbe + (v >> 13) : (v & 0xFFFFu) * a.k.k8 + tbe;   // lower lane: multiply-add
+            ad = (e & 2) ? tbe + (v >> 13) : (v & 0xFFFFu) * a.k.k8 + tbe;   // lower lane: multiply-add
+          } else {
+            ad = tbe + (((e & 1) ? vo[e >> 1] : ve[e >> 1]) << 3);
           }
-          return tbe + (((e & 1) ? vo[e >> 1] : ve[e >> 1]) << 3);
+          SKV_CHECK(ad - tbe < 2048u && tbe + 2048u <= kEncTabBytes, kSiteEncEntry);
+          return ad;
         };
         uint2 ent[G];
 #pragma unroll
@@ -1135,6 +1212,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
           enc_step_smem_fma(x, rp, ent[e], a.k);
         }
       }
+      SKV_CHECK(buf_top - rp <= kEmitBytes, kSiteWordBuffer);
       tc = tn;
       pc = pn;
     }
@@ -1146,6 +1224,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
     sts_u16(rp, x >> 16);
     const uint32_t my_bytes = (uint32_t)(my_slot_end - gp) + (buf_top - rp);
     emit_flush_all(buf_top, rp, gp);
+    SKV_CHECK((uint64_t)(my_slot_end - gp) <= 2 * a.slot_words, kSiteScratchSlot);
     // lane lengths in format-lane order and the chunk total
     const uint32_t len = __shfl_sync(0xFFFFFFFFu, my_bytes, owner_of_tid);
     uint32_t incl = len;
@@ -1327,6 +1406,7 @@ __global__ void __launch_bounds__(dec_threads(PAGED, MODEL), 1) k_decode_kv(Code
       o.w = ESZ == 1 ? unord8x4(pw[3] + sw[3] - kBias) : unord16x2(pw[3] + sw[3] - kBias);
       bool ok;
       const uint64_t oo = goff(i, btc, ok);
+      SKV_CHECK(PAGED || oo + 16 <= (a.n_chunks / a.cps) * a.slice_pos * ESZ, kSiteDecOut);
       if (ok) stg_stream(a.out + oo, o);
       pc = pn;
       if (PAGED) {
@@ -1417,6 +1497,7 @@ __device__ __forceinline__ void coef_group(const CodecArgs& a, uint32_t c, uint3
     G.skip |= (bin == 0xFFu ? 1u : 0u) << e;
     bad |= bin > 63u && bin != 0xFFu;
     G.tbl[e] = 16u * min(bin, 63u) + f;   // a skipped component's table is never read
+    SKV_CHECK(G.tbl[e] < kCoefTables, kSiteCoefTable);
   }
   if (bad) atomicOr(a.status, SKV_FLAG_BAD_BIN);
 }
@@ -1808,15 +1889,19 @@ __global__ void __launch_bounds__(kUmThreads, kUmCtas) k_ctx_umma(const __grid_c
     umma_commit(bar_done);
   }
   __syncwarp();
-  if (!mbar_wait(bar_done, 0)) ok = false;
+  bool done = mbar_wait(bar_done, 0);
+  if (!done) ok = false;
   tc_fence_after();
+  // a wait that ran out anywhere in the CTA: the accumulator is not read and
+  // nothing is stored (the output is undefined; SKV_FLAG_TIMEOUT is set)
+  const bool failed = __syncthreads_or(!ok) != 0;
   // accumulator rows -> floor(acc / 2^s) in the (now idle) stages, row r at r * kUmOutPitch words;
   // warp w reads rows 32 (w mod 4) .. (its tensor-memory lane quarter), columns of part w / 4
   constexpr uint32_t kParts = kUmThreads / 128, kPartCols = kUmBN / kParts;
   const uint32_t q4 = warp & 3, part = warp >> 2;
   const uint32_t srow = base + (q4 * 32 + lane) * kUmOutPitch * 4;
 #pragma unroll 1
-  for (uint32_t c0 = part * kPartCols; c0 < (part + 1) * kPartCols; c0 += 32) {
+  for (uint32_t c0 = part * kPartCols; !failed && c0 < (part + 1) * kPartCols; c0 += 32) {
     uint32_t r[32];
     tmem_ld32(tmem + ((q4 * 32u) << 16) + c0, r);
 #pragma unroll
@@ -1830,7 +1915,15 @@ __global__ void __launch_bounds__(kUmThreads, kUmCtas) k_ctx_umma(const __grid_c
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kUmBN));
+  // tensor memory is freed once every MMA has completed (a second bounded wait if the first ran out)
+  if (warp == 2) {
+    if (!done) done = mbar_wait(bar_done, 0);
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kUmBN));
+  }
+  if (failed) {
+    if (threadIdx.x == 0) atomicOr(status, SKV_FLAG_TIMEOUT);
+    return;
+  }
   // rows out: warp w takes rows w, w + 8, ...; lane l columns 4l..4l+3 (+128);
   // eight rows per step, so that their mu loads are in flight together
   constexpr uint32_t kRows = 8, kWarps = kUmThreads / 32;
@@ -1993,6 +2086,19 @@ __global__ void __launch_bounds__(256) k_compact(const uint16_t* slots, const ui
     for (uint32_t k = lane; k < n; k += 32) d[k] = src[k];
   }
 }
+
+// Host-resident pipeline helpers: a group's lane offsets moved by a signed
+// byte delta (decode: to the group's own stream), or by the running base of
+// the joined stream (encode), which then advances past the group.
+__global__ void k_offsets_shift(uint64_t* offs, uint64_t n, long long delta) {
+  const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) offs[i] = (uint64_t)((long long)offs[i] + delta);
+}
+__global__ void k_offsets_rebase(uint64_t* offs, uint64_t n, const unsigned long long* base) {
+  const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) offs[i] += *base;
+}
+__global__ void k_base_advance(unsigned long long* base, const uint64_t* offs_last) { *base = *offs_last; }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? SKV_OK : SKV_ERR_CUDA; }
 
@@ -2507,6 +2613,293 @@ int skv_selftest_lookback(uint64_t* d_state, uint32_t n_chunks, uint32_t missing
       reinterpret_cast<unsigned long long*>(d_state), n_chunks, missing_chunk, max_spins, d_status,
       reinterpret_cast<unsigned long long*>(d_excl));
   return launch_check();
+}
+
+// ---------------------------------------------------------------------------
+// Host-resident caches: layer groups coded on three streams (copy in, code,
+// copy out), double-buffered device memory from the caller's workspace.
+// ---------------------------------------------------------------------------
+namespace {
+struct HostPlan {
+  Geo g;
+  uint32_t group_layers, n_groups;
+  uint64_t layer_elems, layer_lanes, layer_channels, group_cap;
+  uint64_t in_bytes, off_bytes, ws_enc, total;
+  uint64_t t_off[2], p_off[2], bs_off[2], o_off[2], ws_off, st_off, base_off;
+};
+int host_plan(const skv_params* p, uint32_t group_layers, uint64_t group_cap_bytes, HostPlan* hp) {
+  memset(hp, 0, sizeof(*hp));
+  int st = make_geo(p, &hp->g);
+  if (st != SKV_OK) return st;
+  if (hp->g.dtype == SKV_COEF_I16) return SKV_ERR_UNSUPPORTED;
+  if (group_layers == 0 || p->n_layers == 0) return SKV_ERR_INVALID_ARG;
+  const uint32_t gl = group_layers < p->n_layers ? group_layers : p->n_layers;
+  hp->group_layers = gl;
+  hp->n_groups = (p->n_layers + gl - 1) / gl;
+  hp->layer_elems = (uint64_t)p->n_kv * p->n_heads * p->n_tokens * p->head_dim;
+  hp->layer_lanes = hp->g.n_lanes / p->n_layers;
+  hp->layer_channels = hp->g.n_channels / p->n_layers;
+  skv_params q = *p;
+  q.n_layers = gl;
+  const uint64_t worst = skv_max_bitstream_bytes(&q);
+  uint64_t cap = group_cap_bytes == 0 || group_cap_bytes > worst ? worst : group_cap_bytes;
+  cap = (cap + 16 + 255) & ~255ull;   // + the decoder's read-ahead past the last byte
+  hp->group_cap = cap;
+  hp->in_bytes = align256(hp->layer_elems * gl * hp->g.esz);
+  hp->off_bytes = align256((hp->layer_lanes * gl + 1) * 8);
+  hp->ws_enc = align256(skv_encode_workspace_bytes(&q));
+  uint64_t o = 0;
+  for (int b = 0; b < 2; ++b) {
+    hp->t_off[b] = o; o += hp->in_bytes;
+    hp->p_off[b] = o; o += hp->in_bytes;
+    hp->bs_off[b] = o; o += cap;
+    hp->o_off[b] = o; o += hp->off_bytes;
+  }
+  hp->ws_off = o; o += hp->ws_enc;
+  hp->st_off = o; o += align256(4ull * hp->n_groups);
+  hp->base_off = o; o += 256;
+  hp->total = o;
+  return SKV_OK;
+}
+// combined status of n device words (synchronous)
+int group_statuses(const uint32_t* d_st, uint32_t n, cudaStream_t s) {
+  uint32_t buf[256];
+  int worst = SKV_OK;
+  for (uint32_t i = 0; i < n; i += 256) {
+    const uint32_t m = n - i < 256 ? n - i : 256;
+    int st = cuda_status(cudaMemcpyAsync(buf, d_st + i, 4 * m, cudaMemcpyDeviceToHost, s));
+    if (st == SKV_OK) st = cuda_status(cudaStreamSynchronize(s));
+    if (st != SKV_OK) return st;
+    for (uint32_t k = 0; k < m; ++k) {
+      const uint32_t v = buf[k];
+      const int c = (v & SKV_FLAG_CORRUPT) ? SKV_ERR_CORRUPT : (v & SKV_FLAG_CAPACITY) ? SKV_ERR_CAPACITY
+                    : (v & SKV_FLAG_TIMEOUT) ? SKV_ERR_TIMEOUT : (v & (SKV_FLAG_BAD_BIN | SKV_FLAG_BAD_BLOCK)) ? SKV_ERR_INVALID_ARG
+                    : SKV_OK;
+      if (worst == SKV_OK) worst = c;
+    }
+  }
+  return worst;
+}
+struct Events {
+  cudaEvent_t e[4][2];
+  int n = 0;
+  int create() {
+    for (int i = 0; i < 4; ++i)
+      for (int b = 0; b < 2; ++b) {
+        if (cudaEventCreateWithFlags(&e[i][b], cudaEventDisableTiming) != cudaSuccess) return SKV_ERR_CUDA;
+        ++n;
+      }
+    return SKV_OK;
+  }
+  ~Events() {
+    for (int k = 0; k < n; ++k) cudaEventDestroy(e[k / 2][k % 2]);
+  }
+};
+}  // namespace
+
+uint64_t skv_host_workspace_bytes(const skv_params* p, uint32_t group_layers, uint64_t group_cap_bytes) {
+  HostPlan hp;
+  return host_plan(p, group_layers, group_cap_bytes, &hp) == SKV_OK ? hp.total : 0;
+}
+
+int skv_encode_host(const skv_params* p, const void* h_target, const void* h_pred, const void* d_tables,
+                    uint8_t* d_bins, void* h_bitstream, uint64_t cap_bytes, uint64_t* h_lane_offsets,
+                    uint64_t* h_total_bytes, uint32_t group_layers, uint64_t group_cap_bytes, void* d_workspace,
+                    uint64_t workspace_bytes, void* const* streams) {
+  HostPlan hp;
+  int st = host_plan(p, group_layers, group_cap_bytes, &hp);
+  if (st != SKV_OK) return st;
+  if (!h_target || !h_pred || !d_tables || !d_bins || !h_bitstream || !h_lane_offsets || !d_workspace || !streams ||
+      !aligned16(d_workspace) || !aligned16(d_tables) || !aligned16(d_bins) || workspace_bytes < hp.total)
+    return SKV_ERR_INVALID_ARG;
+  cudaStream_t s_in = static_cast<cudaStream_t>(streams[0]), s_c = static_cast<cudaStream_t>(streams[1]),
+               s_out = static_cast<cudaStream_t>(streams[2]);
+  Events ev;   // [0] inputs copied, [1] group coded, [2] offsets copied out, [3] stream copied out
+  if ((st = ev.create()) != SKV_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(d_workspace);
+  uint32_t* d_st = reinterpret_cast<uint32_t*>(ws + hp.st_off);
+  unsigned long long* d_base = reinterpret_cast<unsigned long long*>(ws + hp.base_off);
+  const uint32_t G = hp.n_groups, esz = hp.g.esz;
+  const uint8_t* ht = static_cast<const uint8_t*>(h_target);
+  const uint8_t* hpd = static_cast<const uint8_t*>(h_pred);
+  uint8_t* hbs = static_cast<uint8_t*>(h_bitstream);
+  if ((st = cuda_status(cudaMemsetAsync(d_base, 0, 8, s_c))) != SKV_OK) return st;
+  if ((st = cuda_status(cudaMemsetAsync(d_st, 0, 4ull * G, s_c))) != SKV_OK) return st;
+  auto lo_of = [&](uint32_t k) { return (uint64_t)k * hp.group_layers; };
+  auto nl_of = [&](uint32_t k) {
+    const uint64_t lo = lo_of(k);
+    return (uint32_t)((lo + hp.group_layers <= p->n_layers ? hp.group_layers : p->n_layers - lo));
+  };
+  cudaEvent_t ev_first;
+  if (cudaEventCreateWithFlags(&ev_first, cudaEventDisableTiming) != cudaSuccess) return SKV_ERR_CUDA;
+  cudaEventRecord(ev_first, s_c);   // the memsets above come first on every stream
+  cudaStreamWaitEvent(s_in, ev_first, 0);
+  cudaStreamWaitEvent(s_out, ev_first, 0);
+  auto copy_in = [&](uint32_t k) -> int {
+    const uint32_t b = k & 1u;
+    if (k >= 2 && cudaStreamWaitEvent(s_in, ev.e[1][b], 0) != cudaSuccess) return SKV_ERR_CUDA;
+    const uint64_t n = hp.layer_elems * nl_of(k) * esz, off = hp.layer_elems * lo_of(k) * esz;
+    if (cudaMemcpyAsync(ws + hp.t_off[b], ht + off, n, cudaMemcpyHostToDevice, s_in) != cudaSuccess ||
+        cudaMemcpyAsync(ws + hp.p_off[b], hpd + off, n, cudaMemcpyHostToDevice, s_in) != cudaSuccess ||
+        cudaEventRecord(ev.e[0][b], s_in) != cudaSuccess)
+      return SKV_ERR_CUDA;
+    return SKV_OK;
+  };
+  // the group's stream out to the host at the base the device computed (the
+  // host reads it from the group's copied offsets: one group behind)
+  auto copy_stream_out = [&](uint32_t k) -> int {
+    const uint32_t b = k & 1u;
+    if (cudaEventSynchronize(ev.e[2][b]) != cudaSuccess) return SKV_ERR_CUDA;
+    const uint64_t l0 = hp.layer_lanes * lo_of(k), nl = hp.layer_lanes * nl_of(k);
+    const uint64_t a0 = h_lane_offsets[l0], a1 = h_lane_offsets[l0 + nl];
+    if (a1 < a0 || a1 - a0 > hp.group_cap - 16) return SKV_ERR_CAPACITY;
+    if (a1 > cap_bytes) return SKV_ERR_CAPACITY;
+    if (cudaMemcpyAsync(hbs + a0, ws + hp.bs_off[b], a1 - a0, cudaMemcpyDeviceToHost, s_out) != cudaSuccess ||
+        cudaEventRecord(ev.e[3][b], s_out) != cudaSuccess)
+      return SKV_ERR_CUDA;
+    return SKV_OK;
+  };
+  if ((st = copy_in(0)) != SKV_OK) goto done;
+  for (uint32_t k = 0; k < G; ++k) {
+    const uint32_t b = k & 1u;
+    if (k + 1 < G && (st = copy_in(k + 1)) != SKV_OK) goto done;
+    {
+      skv_params q = *p;
+      q.n_layers = nl_of(k);
+      const uint64_t nlanes = hp.layer_lanes * q.n_layers;
+      uint64_t* d_off = reinterpret_cast<uint64_t*>(ws + hp.o_off[b]);
+      if (cudaStreamWaitEvent(s_c, ev.e[0][b], 0) != cudaSuccess ||
+          (k >= 2 && cudaStreamWaitEvent(s_c, ev.e[3][b], 0) != cudaSuccess)) {
+        st = SKV_ERR_CUDA;
+        goto done;
+      }
+      uint8_t* bins_k = d_bins + hp.layer_channels * lo_of(k);
+      if ((st = skv_calibrate(&q, ws + hp.t_off[b], ws + hp.p_off[b], bins_k, nullptr, nullptr, s_c)) != SKV_OK) goto done;
+      if ((st = encode_impl(&q, nullptr, ws + hp.t_off[b], ws + hp.p_off[b], d_tables, bins_k, ws + hp.bs_off[b],
+                            hp.group_cap - 16, d_off, ws + hp.ws_off, hp.ws_enc, d_st + k, nullptr, s_c)) != SKV_OK)
+        goto done;
+      const unsigned nb = (unsigned)((nlanes + 1 + 255) / 256);
+      k_offsets_rebase<<<nb, 256, 0, s_c>>>(d_off, nlanes + 1, d_base);
+      k_base_advance<<<1, 1, 0, s_c>>>(d_base, d_off + nlanes);
+      if ((st = launch_check()) != SKV_OK || cudaEventRecord(ev.e[1][b], s_c) != cudaSuccess) {
+        st = st != SKV_OK ? st : SKV_ERR_CUDA;
+        goto done;
+      }
+      if (cudaStreamWaitEvent(s_out, ev.e[1][b], 0) != cudaSuccess ||
+          cudaMemcpyAsync(h_lane_offsets + hp.layer_lanes * lo_of(k), d_off, 8 * (nlanes + 1), cudaMemcpyDeviceToHost,
+                          s_out) != cudaSuccess ||
+          cudaEventRecord(ev.e[2][b], s_out) != cudaSuccess) {
+        st = SKV_ERR_CUDA;
+        goto done;
+      }
+    }
+    if (k >= 1 && (st = copy_stream_out(k - 1)) != SKV_OK) goto done;
+  }
+  st = copy_stream_out(G - 1);
+done:
+  {
+    // drain all three streams before the events and buffers go away
+    const int s1 = cuda_status(cudaStreamSynchronize(s_in)), s2 = cuda_status(cudaStreamSynchronize(s_c)),
+              s3 = cuda_status(cudaStreamSynchronize(s_out));
+    cudaEventDestroy(ev_first);
+    if (st == SKV_OK) st = s1 != SKV_OK ? s1 : (s2 != SKV_OK ? s2 : s3);
+  }
+  if (st == SKV_OK) st = group_statuses(d_st, G, s_c);
+  if (st == SKV_OK && h_total_bytes) *h_total_bytes = h_lane_offsets[hp.g.n_lanes];
+  return st;
+}
+
+int skv_decode_host(const skv_params* p, const void* h_bitstream, uint64_t n_bytes, const uint64_t* h_lane_offsets,
+                    const void* h_pred, const void* d_tables, const uint8_t* d_bins, void* h_target_out,
+                    uint32_t group_layers, uint64_t group_cap_bytes, void* d_workspace, uint64_t workspace_bytes,
+                    void* const* streams) {
+  HostPlan hp;
+  int st = host_plan(p, group_layers, group_cap_bytes, &hp);
+  if (st != SKV_OK) return st;
+  if (!h_bitstream || !h_lane_offsets || !h_pred || !d_tables || !d_bins || !h_target_out || !d_workspace ||
+      !streams || !aligned16(d_workspace) || !aligned16(d_tables) || !aligned16(d_bins) ||
+      workspace_bytes < hp.total)
+    return SKV_ERR_INVALID_ARG;
+  if (h_lane_offsets[0] != 0 || h_lane_offsets[hp.g.n_lanes] != n_bytes) return SKV_ERR_CORRUPT;
+  cudaStream_t s_in = static_cast<cudaStream_t>(streams[0]), s_c = static_cast<cudaStream_t>(streams[1]),
+               s_out = static_cast<cudaStream_t>(streams[2]);
+  Events ev;   // [0] inputs copied, [1] group decoded, [2] target copied out
+  if ((st = ev.create()) != SKV_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(d_workspace);
+  uint32_t* d_st = reinterpret_cast<uint32_t*>(ws + hp.st_off);
+  const uint32_t G = hp.n_groups, esz = hp.g.esz;
+  const uint8_t* hbs = static_cast<const uint8_t*>(h_bitstream);
+  const uint8_t* hpd = static_cast<const uint8_t*>(h_pred);
+  uint8_t* hto = static_cast<uint8_t*>(h_target_out);
+  auto lo_of = [&](uint32_t k) { return (uint64_t)k * hp.group_layers; };
+  auto nl_of = [&](uint32_t k) {
+    const uint64_t lo = lo_of(k);
+    return (uint32_t)((lo + hp.group_layers <= p->n_layers ? hp.group_layers : p->n_layers - lo));
+  };
+  // every group's stream must fit its buffer (checked before anything is launched)
+  for (uint32_t k = 0; k < G; ++k) {
+    const uint64_t l0 = hp.layer_lanes * lo_of(k), nl = hp.layer_lanes * nl_of(k);
+    const uint64_t a0 = h_lane_offsets[l0], a1 = h_lane_offsets[l0 + nl];
+    if (a1 < a0 || a1 > n_bytes) return SKV_ERR_CORRUPT;
+    if (a1 - a0 > hp.group_cap - 16) return SKV_ERR_CAPACITY;
+  }
+  for (uint32_t k = 0; k < G; ++k) {
+    const uint32_t b = k & 1u;
+    skv_params q = *p;
+    q.n_layers = nl_of(k);
+    const uint64_t l0 = hp.layer_lanes * lo_of(k), nlanes = hp.layer_lanes * q.n_layers;
+    const uint64_t a0 = h_lane_offsets[l0], a1 = h_lane_offsets[l0 + nlanes];
+    const uint64_t n = hp.layer_elems * q.n_layers * esz, off = hp.layer_elems * lo_of(k) * esz;
+    uint64_t* d_off = reinterpret_cast<uint64_t*>(ws + hp.o_off[b]);
+    // in: prediction, the group's stream and its offsets (moved to the group's own stream)
+    if ((k >= 2 && cudaStreamWaitEvent(s_in, ev.e[1][b], 0) != cudaSuccess) ||
+        cudaMemcpyAsync(ws + hp.p_off[b], hpd + off, n, cudaMemcpyHostToDevice, s_in) != cudaSuccess ||
+        cudaMemcpyAsync(ws + hp.bs_off[b], hbs + a0, a1 - a0, cudaMemcpyHostToDevice, s_in) != cudaSuccess ||
+        cudaMemcpyAsync(d_off, h_lane_offsets + l0, 8 * (nlanes + 1), cudaMemcpyHostToDevice, s_in) != cudaSuccess ||
+        cudaEventRecord(ev.e[0][b], s_in) != cudaSuccess) {
+      st = SKV_ERR_CUDA;
+      break;
+    }
+    if (cudaStreamWaitEvent(s_c, ev.e[0][b], 0) != cudaSuccess ||
+        (k >= 2 && cudaStreamWaitEvent(s_c, ev.e[2][b], 0) != cudaSuccess)) {
+      st = SKV_ERR_CUDA;
+      break;
+    }
+    k_offsets_shift<<<(unsigned)((nlanes + 1 + 255) / 256), 256, 0, s_c>>>(d_off, nlanes + 1, -(long long)a0);
+    if ((st = launch_check()) != SKV_OK) break;
+    if ((st = decode_impl(&q, nullptr, ws + hp.bs_off[b], a1 - a0, d_off, ws + hp.p_off[b], d_tables,
+                          d_bins + hp.layer_channels * lo_of(k), ws + hp.t_off[b], d_st + k, s_c)) != SKV_OK)
+      break;
+    if (cudaEventRecord(ev.e[1][b], s_c) != cudaSuccess || cudaStreamWaitEvent(s_out, ev.e[1][b], 0) != cudaSuccess ||
+        cudaMemcpyAsync(hto + off, ws + hp.t_off[b], n, cudaMemcpyDeviceToHost, s_out) != cudaSuccess ||
+        cudaEventRecord(ev.e[2][b], s_out) != cudaSuccess) {
+      st = SKV_ERR_CUDA;
+      break;
+    }
+  }
+  const int s1 = cuda_status(cudaStreamSynchronize(s_in)), s2 = cuda_status(cudaStreamSynchronize(s_c)),
+            s3 = cuda_status(cudaStreamSynchronize(s_out));
+  if (st == SKV_OK) st = s1 != SKV_OK ? s1 : (s2 != SKV_OK ? s2 : s3);
+  if (st == SKV_OK) st = group_statuses(d_st, G, s_c);
+  return st;
+}
+
+int skv_checked_failures(uint32_t* h_count, uint32_t* h_first_site) {
+#if SKV_CHECKED
+  if (!h_count || !h_first_site) return SKV_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SKV_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(h_count, g_check_count, 4) != cudaSuccess ||
+      cudaMemcpyFromSymbol(h_first_site, g_check_site, 4) != cudaSuccess)
+    return SKV_ERR_CUDA;
+  const uint32_t z = 0;
+  if (cudaMemcpyToSymbol(g_check_count, &z, 4) != cudaSuccess || cudaMemcpyToSymbol(g_check_site, &z, 4) != cudaSuccess)
+    return SKV_ERR_CUDA;
+  return SKV_OK;
+#else
+  (void)h_count;
+  (void)h_first_site;
+  return SKV_ERR_UNSUPPORTED;
+#endif
 }
 
 int skv_read_status(const uint32_t* d_status, void* stream) {

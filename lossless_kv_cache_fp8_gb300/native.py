@@ -110,24 +110,50 @@ _SIGS = {
     "skv_decode_paged": (C.c_int, [_P, _PL, C.c_void_p, C.c_uint64, C.c_void_p, C.c_void_p, C.c_void_p,
                                    C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
     "skv_ctx_scratch_bytes": (C.c_uint64, [C.c_uint64, C.c_uint32, C.c_uint32]),
+    "skv_host_workspace_bytes": (C.c_uint64, [_P, C.c_uint32, C.c_uint64]),
+    "skv_checked_failures": (C.c_int, [C.c_void_p, C.c_void_p]),
+    "skv_encode_host": (C.c_int, [_P, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_uint64,
+                                  C.c_void_p, C.c_void_p, C.c_uint32, C.c_uint64, C.c_void_p, C.c_uint64,
+                                  C.c_void_p]),
+    "skv_decode_host": (C.c_int, [_P, C.c_void_p, C.c_uint64, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                  C.c_void_p, C.c_uint32, C.c_uint64, C.c_void_p, C.c_uint64, C.c_void_p]),
     "skv_ctx_means": (C.c_int, [_CM, C.c_void_p, C.c_uint64, C.c_void_p, C.c_uint64, C.c_uint32, C.c_void_p,
                                 C.c_void_p, C.c_uint64, C.c_void_p, C.c_void_p]),
 }
+
+
+def load(path: str):
+    """load a build of the library (the ordinary one, or the checked one) with
+    its function signatures"""
+    if not os.path.exists(path):
+        raise ImportError(f"{os.path.basename(path)} not built ({path}); run __graft_entry__.build()")
+    L = C.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
 
 
 def lib():
     """Load libskv.so; raises if it has not been built."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise ImportError(f"libskv.so not built ({LIB_PATH}); run __graft_entry__.build()")
-        L = C.CDLL(LIB_PATH)
-        for name, (res, args) in _SIGS.items():
-            fn = getattr(L, name)
-            fn.restype = res
-            fn.argtypes = args
-        _lib = L
+        _lib = load(LIB_PATH)
     return _lib
+
+
+def use_library(path: str | None):
+    """route every call of this module to another build (None: libskv.so again)"""
+    global _lib
+    _lib = None if path is None else load(path)
+
+
+def skv_checked_failures():
+    """(status, count, first site) of the checked build's failed checks (cleared)"""
+    n, site = C.c_uint32(0), C.c_uint32(0)
+    st = lib().skv_checked_failures(C.byref(n), C.byref(site))
+    return st, n.value, site.value
 
 
 def header_functions() -> list[str]:
@@ -222,6 +248,34 @@ def skv_selftest_ctx_wait(scratch, status, stream=None) -> int:
 def skv_selftest_lookback(state, n_chunks, missing_chunk, max_spins, excl, status, stream=None) -> int:
     return lib().skv_selftest_lookback(_ptr(state), n_chunks, missing_chunk, max_spins, _ptr(excl), _ptr(status),
                                        _stream(stream))
+
+
+def _streams3(streams):
+    """array of three cudaStream_t (copy in, code, copy out) for the host calls"""
+    arr = (C.c_void_p * 3)(*[_stream(s) for s in streams])
+    return arr
+
+
+def skv_host_workspace_bytes(p, group_layers: int, group_cap_bytes: int = 0) -> int:
+    return lib().skv_host_workspace_bytes(C.byref(p), group_layers, group_cap_bytes)
+
+
+def skv_encode_host(p, h_target, h_pred, tables, bins, h_bitstream, cap_bytes, h_lane_offsets, group_layers,
+                    group_cap_bytes, workspace, streams):
+    """returns (status, total bytes); synchronous"""
+    total = C.c_uint64(0)
+    st = lib().skv_encode_host(C.byref(p), _ptr(h_target), _ptr(h_pred), _ptr(tables), _ptr(bins),
+                               _ptr(h_bitstream), cap_bytes, _ptr(h_lane_offsets), C.byref(total), group_layers,
+                               group_cap_bytes, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               _streams3(streams))
+    return st, total.value
+
+
+def skv_decode_host(p, h_bitstream, n_bytes, h_lane_offsets, h_pred, tables, bins, h_target_out, group_layers,
+                    group_cap_bytes, workspace, streams) -> int:
+    return lib().skv_decode_host(C.byref(p), _ptr(h_bitstream), n_bytes, _ptr(h_lane_offsets), _ptr(h_pred),
+                                 _ptr(tables), _ptr(bins), _ptr(h_target_out), group_layers, group_cap_bytes,
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(), _streams3(streams))
 
 
 def skv_read_status(status, stream=None) -> int:

@@ -62,3 +62,27 @@ def gather_totals(local_total: int, group=None):
     out = [torch.zeros_like(t) for _ in range(world)]
     dist.all_gather(out, t, group=group)
     return [int(x.item()) for x in out]
+
+
+def encode_layer_shard(params, target, pred, lo: int, hi: int, group=None, device=None, cap_frac: float = 1.0):
+    """One rank's part of a sharded encode through the CUDA library: calibrate,
+    build the tables and encode layers [lo, hi) (``target`` / ``pred`` hold only
+    those layers, on this rank's GPU), then all-gather the byte totals.
+
+    Returns (codec, n_bytes, base, totals): the shard's stream is
+    ``codec.bitstream[:n_bytes]`` and belongs at byte ``base`` of the joined
+    stream; its lane offsets plus ``base`` are the joined offsets of its lanes
+    (lanes are numbered layer-major, so shard r's lanes follow shard r-1's)."""
+    from . import native
+    q = shard_params(params, lo, hi)
+    raw = target.numel() * target.element_size()
+    cap = None if cap_frac >= 1.0 else max(4096, int(raw * cap_frac))
+    codec = native.Codec(q, device=device or target.device, bitstream_capacity=cap)
+    codec.calibrate(target, pred)
+    codec.build_tables()
+    n = codec.encode(target, pred, want_total=True)
+    native._check(codec.check(), "skv_encode (shard)")
+    totals = gather_totals(n, group)
+    import torch.distributed as dist
+    rank = dist.get_rank(group)
+    return codec, n, int(shard_bases(totals)[rank]), totals
