@@ -443,6 +443,18 @@ __device__ __forceinline__ uint4 load_block(const RingLane& L, uint32_t k) {
   return k <= L.last ? ldg_stream(L.base + ((uint64_t)k << 4)) : make_uint4(0, 0, 0, 0);
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// asynchronous 4- / 8-byte copies from global memory to the dynamic shared
+// array at byte offset a (waited for by cp_async_wait_all)
+__device__ __forceinline__ void cp_async_4(uint32_t a, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(g_smem + a)),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_8(uint32_t a, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"((uint32_t)__cvta_generic_to_shared(g_smem + a)),
+               "l"(src)
+               : "memory");
+}
 // block rb -> ring slot rb mod 4 (zero bytes read past the lane's last block)
 __device__ __forceinline__ void ring_step(RingLane& L) {
   const uint32_t saddr = (uint32_t)__cvta_generic_to_shared(g_smem + L.ring + (L.rb & 3u) * 16u);
@@ -787,6 +799,7 @@ struct CodecArgs {
   uint8_t* out_bs;                  // final bitstream
   uint64_t cap;
   uint64_t slot_warps;              // warps that own a slot set in the workspace
+  uint64_t last_wave;               // chunks from here on are the last wave handed out
   Paged pg;                         // paged pools (pg.bt == nullptr: dense caches)
   PipeConsts k;                     // 4096, 0xFFFFFFFF, 2^20, 8 (see PipeConsts)
 };
@@ -847,6 +860,45 @@ __device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
+}
+
+// ---- mbarriers (shared memory, one arrival + transaction bytes) ----------
+constexpr uint64_t kBarWaitNs = 1000000000ull;   // ~1 s bound on every barrier wait
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// wait for the phase of parity `parity` to complete; false after ~1 s
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try(bar, parity))
+    if (global_ns() - t0 > kBarWaitNs) return false;
+  return true;
+}
+// bulk copy of `bytes` (a multiple of 16) from global src to shared dst, both
+// 16-byte aligned, completing its bytes on `bar`
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
 }
 
 // ---- decoupled look-back over chunks -------------------------------------
@@ -989,22 +1041,81 @@ __device__ __forceinline__ void warp_copy_words(uint16_t* dst, const uint16_t* s
   if ((n_w & 1) && tid == 0) dst[n_w - 1] = src[n_w - 1];
 }
 
-// Place a coded chunk whose total is published (whole warp calls): resolve
-// its byte offset, write its lane offsets, copy its 32 lane streams from the
-// slot set `sset` into the bitstream.  len / incl are this thread's format
-// lane length and inclusive prefix within the chunk.
-__device__ __noinline__ void place_chunk(const CodecArgs& a, unsigned long long chunk, unsigned long long total,
-                                         uint32_t len, uint32_t incl, uint64_t sset, uint32_t CS, uint32_t R) {
+// A chunk's lanes are copied from their scratch slots into the stream in
+// one of two ways.  While other chunks are still being coded, the copy above
+// runs lane after lane: its memory latency is hidden by the SM's other warps
+// and it costs no shared-memory cycles, which coding needs.  Placements made
+// once the last chunks have been handed out have no such cover, so chunks of
+// at most kStagedMaxBytes (a few staging rounds instead of 32 lane round
+// trips) copy through staging slots (the warp's word buffers, idle between
+// chunks); larger chunks measured faster with the lane-by-lane copy.  Each
+// lane's source bytes, widened to whole 16-byte blocks (the slot ends on a
+// block boundary), are cut into pieces of at most kCpPiece bytes; up to
+// kCpSlots pieces are in flight at once as bulk copies, each completing on its
+// own mbarrier, so the chunk costs a few memory round trips instead of one
+// per lane.  A landed piece is written out as aligned 16-byte destination
+// blocks, each assembled from two 16-byte shared-memory reads shifted by the
+// piece's (even) byte offset; the 16-bit words at either end that share a
+// destination block with another piece, lane or chunk are written one by one.
+constexpr uint32_t kCpSlots = 4, kCpPiece = 1024, kCpStride = 1152;
+constexpr uint32_t kStagedMaxBytes = 32768;
+static_assert(kCpSlots * kCpStride <= kLanes * kEmitBytes, "staging slots fit in a warp's word buffers");
+static_assert(kCpStride >= kCpPiece + 16 && kCpStride % 16 == 0, "the shifted block reads end 16 bytes past a piece");
+static_assert(kCpSlots <= 32, "one descriptor-holding thread per slot");
+constexpr uint32_t kEncWarpExtra = kCpSlots * 8;   // a warp's staging mbarriers, after all the word buffers
+// shared-memory byte offsets of warp w's staging slots (its word buffers) and mbarriers
+__device__ __forceinline__ uint32_t enc_stage_at(uint32_t w) { return kEncTabBytes + w * (kLanes * kEmitBytes); }
+__device__ __forceinline__ uint32_t enc_bars_at(uint32_t w, uint32_t threads) {
+  return kEncTabBytes + threads * kEmitBytes + w * kEncWarpExtra;
+}
+__host__ __device__ constexpr uint32_t enc_smem_bytes(uint32_t threads) {
+  return kEncTabBytes + threads * kEmitBytes + threads / 32 * kEncWarpExtra;
+}
+static_assert(enc_smem_bytes(kEncThreads) <= 227 * 1024, "the encoder's shared memory fits one CTA per SM");
+constexpr uint32_t kPlaceFailed = 1u << 31;       // place_chunk: a staging wait gave up
+
+// 16 destination bytes from the 32 staged bytes w[0..7] starting at byte
+// 4 q + 2 h (q, h warp-uniform)
+__device__ __forceinline__ uint4 shift_block(const uint4& lo, const uint4& hi, uint32_t q, uint32_t h) {
+  const uint32_t sh = h ? 16u : 0u;
+  uint32_t v0, v1, v2, v3, v4;
+  if (q == 0) { v0 = lo.x; v1 = lo.y; v2 = lo.z; v3 = lo.w; v4 = hi.x; }
+  else if (q == 1) { v0 = lo.y; v1 = lo.z; v2 = lo.w; v3 = hi.x; v4 = hi.y; }
+  else if (q == 2) { v0 = lo.z; v1 = lo.w; v2 = hi.x; v3 = hi.y; v4 = hi.z; }
+  else { v0 = lo.w; v1 = hi.x; v2 = hi.y; v3 = hi.z; v4 = hi.w; }
+  return make_uint4(__funnelshift_r(v0, v1, sh), __funnelshift_r(v1, v2, sh), __funnelshift_r(v2, v3, sh),
+                    __funnelshift_r(v3, v4, sh));
+}
+
+// Resolve a coded chunk's byte offset (its total is published) and write its
+// lane offsets (whole warp calls).  Returns this thread's format lane's
+// stream offset, or ~0 when the chunk is not to be copied (a failed wait or
+// a stream past the capacity, both flagged).
+__device__ __forceinline__ unsigned long long chunk_lane_offset(const CodecArgs& a, unsigned long long chunk,
+                                                                unsigned long long total, uint32_t len,
+                                                                uint32_t incl) {
   const uint32_t tid = threadIdx.x & 31;
   const unsigned long long excl = chunk_resolve(a.chunk_state, chunk, total, a.status, kMaxSpins);
-  if (excl == ~0ull) return;
+  if (excl == ~0ull) return ~0ull;
   const unsigned long long lane_off = excl + incl - len;
   a.lane_offsets[chunk * kLanes + tid] = lane_off;
   if (chunk + 1 == a.n_chunks && tid == 31) a.lane_offsets[a.n_lanes] = excl + total;
   if (excl + total > a.cap) {
     if (tid == 0) atomicOr(a.status, SKV_FLAG_CAPACITY);
-    return;
+    return ~0ull;
   }
+  return lane_off;
+}
+
+// Place a coded chunk whose total is published (whole warp calls): resolve
+// its byte offset, write its lane offsets, copy its 32 lane streams from the
+// slot set `sset` into the bitstream lane after lane.  len / incl are this
+// thread's format lane length and inclusive prefix within the chunk.
+__device__ __forceinline__ void place_chunk(const CodecArgs& a, unsigned long long chunk, unsigned long long total,
+                                            uint32_t len, uint32_t incl, uint64_t sset, uint32_t CS, uint32_t R) {
+  const uint32_t tid = threadIdx.x & 31;
+  const unsigned long long lane_off = chunk_lane_offset(a, chunk, total, len, incl);
+  if (lane_off == ~0ull) return;
   __syncwarp();
   for (uint32_t l = 0; l < kLanes; ++l) {
     const uint32_t n_w = __shfl_sync(0xFFFFFFFFu, len, l) >> 1;
@@ -1018,6 +1129,131 @@ __device__ __noinline__ void place_chunk(const CodecArgs& a, unsigned long long 
   __syncwarp();
 }
 
+// The same through the staging slots.  phase: the next parities of the
+// warp's staging mbarriers, returned updated, with kPlaceFailed set if a wait
+// gave up (status flagged, every copy waited for).
+__device__ __forceinline__ uint32_t place_chunk_staged(const CodecArgs& a, unsigned long long chunk,
+                                                       unsigned long long total, uint32_t len, uint32_t incl,
+                                                       uint64_t sset, uint32_t CS, uint32_t R, uint32_t phase) {
+  const uint32_t tid = threadIdx.x & 31;
+  const unsigned long long lane_off = chunk_lane_offset(a, chunk, total, len, incl);
+  if (lane_off == ~0ull) return phase;
+  const uint32_t owner = (tid % CS) * R + tid / CS;
+  const uint8_t* end = reinterpret_cast<const uint8_t*>(a.slots + (sset * kLanes + owner + 1) * a.slot_words);
+  SKV_CHECK(lane_off + len <= a.cap && len <= 2 * a.slot_words, kSiteStreamCopy);
+  const uint32_t span = min((len + 15u) & ~15u, (uint32_t)(2 * a.slot_words));   // aligned source bytes
+  const uint32_t np = (span + kCpPiece - 1) / kCpPiece;
+  uint32_t pincl = np;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xFFFFFFFFu, pincl, o);
+    if (tid >= (uint32_t)o) pincl += u;
+  }
+  const uint32_t n_pieces = __shfl_sync(0xFFFFFFFFu, pincl, 31);
+  const uint32_t sbase = smem_addr(g_smem);
+  const uint32_t stage = enc_stage_at(threadIdx.x >> 5), bars = enc_bars_at(threadIdx.x >> 5, blockDim.x);
+  // the slots were written, and the staging area (the word buffers) last
+  // read, by this warp's ordinary accesses; the bulk copies go through the
+  // asynchronous proxy
+  asm volatile("fence.proxy.async;" ::: "memory");
+  __syncwarp();
+  // thread s keeps the write-out of the piece in slot s: destination start
+  // (an address: the stream itself need only be 2-byte aligned), staged
+  // offset of its first byte, byte count
+  unsigned long long my_d0 = 0;
+  uint32_t my_s0 = 0, my_n = 0;
+  uint32_t q_in = 0;
+  auto slot_at = [&](uint32_t slot) -> uint32_t { return stage + slot * kCpStride; };
+  auto issue = [&]() {
+    // piece q_in: its lane is the number of lanes whose inclusive piece count is at most q_in
+    const uint32_t l = __popc(__ballot_sync(0xFFFFFFFFu, pincl <= q_in)) & 31u;
+    const uint32_t k = q_in - __shfl_sync(0xFFFFFFFFu, pincl - np, l);
+    const uint32_t sp = __shfl_sync(0xFFFFFFFFu, span, l);
+    const uint32_t len_l = __shfl_sync(0xFFFFFFFFu, len, l);
+    const unsigned long long dst_l = __shfl_sync(0xFFFFFFFFu, lane_off, l);
+    const uint8_t* end_l = reinterpret_cast<const uint8_t*>(
+        __shfl_sync(0xFFFFFFFFu, reinterpret_cast<unsigned long long>(end), l));
+    const uint32_t lo = k * kCpPiece, bytes = min(kCpPiece, sp - lo);   // source bytes [lo, lo + bytes) of the span
+    const uint32_t pad = sp - len_l;                                    // span bytes before the lane's first byte
+    const uint32_t v0 = lo > pad ? lo : pad;                            // first lane byte in the piece
+    const uint32_t slot = q_in % kCpSlots;
+    const uint8_t* src = end_l - sp + lo;
+    const uint32_t sa = slot_at(slot);
+    SKV_CHECK(SKV_SMEM_OK(sa, 16, kSiteStreamCopy) && SKV_SMEM_OK(sa + kCpStride - 16, 16, kSiteStreamCopy) &&
+                  bytes % 16 == 0 &&
+                  bytes <= kCpPiece && pad < 16 && sp <= 2 * a.slot_words,
+              kSiteStreamCopy);
+    if (tid == slot) {
+      my_d0 = reinterpret_cast<unsigned long long>(a.out_bs) + dst_l + (v0 - pad);
+      my_s0 = sa + (v0 - lo);
+      my_n = lo + bytes - v0;
+    }
+    if (tid == 0) {
+      mbar_expect_tx(sbase + bars + 8 * slot, bytes);
+      bulk_g2s(sbase + sa, src, bytes, sbase + bars + 8 * slot);
+    }
+    ++q_in;
+  };
+  while (q_in < n_pieces && q_in < kCpSlots) issue();
+  uint32_t q = 0;
+  for (; q < n_pieces; ++q) {
+    const uint32_t slot = q % kCpSlots;
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(sbase + bars + 8 * slot, (phase >> slot) & 1u))) break;
+    phase ^= 1u << slot;
+    const unsigned long long d0 = __shfl_sync(0xFFFFFFFFu, my_d0, slot);
+    const uint32_t s0 = __shfl_sync(0xFFFFFFFFu, my_s0, slot);
+    const uint32_t n = __shfl_sync(0xFFFFFFFFu, my_n, slot);
+    const unsigned long long d1 = d0 + n;
+    const unsigned long long da = (d0 + 15) & ~15ull, db = d1 & ~15ull;
+    if (da < db) {
+      // whole destination blocks [da, db), staged from s0 + (da - d0)
+      const uint32_t sa = s0 + (uint32_t)(da - d0);
+      const uint32_t base = sa & ~15u, q4 = (sa >> 2) & 3u, h = (sa >> 1) & 1u;
+      const uint32_t nb = (uint32_t)((db - da) >> 4);
+      uint4* dst = reinterpret_cast<uint4*>(da);
+      for (uint32_t i = tid; i < nb; i += 32) {
+        const uint4 lo4 = lds_u128(base + 16 * i), hi4 = lds_u128(base + 16 * i + 16);
+        __stcs(dst + i, shift_block(lo4, hi4, q4, h));
+      }
+      // the 16-bit words before da and from db on
+      const uint32_t nh = (uint32_t)(da - d0) >> 1, nt = (uint32_t)(d1 - db) >> 1;
+      if (tid < nh) *reinterpret_cast<uint16_t*>(d0 + 2 * tid) = (uint16_t)lds_u16(s0 + 2 * tid);
+      else if (tid >= 8 && tid - 8 < nt)
+        *reinterpret_cast<uint16_t*>(db + 2 * (tid - 8)) = (uint16_t)lds_u16(s0 + (uint32_t)(db - d0) + 2 * (tid - 8));
+    } else {
+      // fewer than two blocks' worth: 16-bit words only
+      for (uint32_t i = tid; i < (n >> 1); i += 32)
+        *reinterpret_cast<uint16_t*>(d0 + 2 * i) = (uint16_t)lds_u16(s0 + 2 * i);
+    }
+    // every read of the slot is done before the next bulk copy overwrites it
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (q_in < n_pieces) issue();
+  }
+  if (q < n_pieces) {
+    // a wait gave up: flag it, then wait (bounded) for the copies still in flight
+    if (tid == 0) atomicOr(a.status, SKV_FLAG_TIMEOUT);
+    for (; q < q_in; ++q) {
+      const uint32_t slot = q % kCpSlots;
+      __all_sync(0xFFFFFFFFu, mbar_wait(sbase + bars + 8 * slot, (phase >> slot) & 1u));
+      phase ^= 1u << slot;
+    }
+    return phase | kPlaceFailed;
+  }
+  return phase;
+}
+
+// Place the warp's pending chunk (whole warp calls): through the staging
+// slots when no later chunk is left to hand out (last) and the chunk is
+// small enough, lane after lane otherwise.  Returns the staging mbarriers'
+// parities (see place_chunk_staged).
+__device__ __noinline__ uint32_t place_pending(const CodecArgs& a, unsigned long long chunk, unsigned long long total,
+                                               uint32_t len, uint32_t incl, uint64_t sset, uint32_t CS, uint32_t R,
+                                               bool last, uint32_t phase) {
+  if (last && total <= kStagedMaxBytes) return place_chunk_staged(a, chunk, total, len, incl, sset, CS, R, phase);
+  place_chunk(a, chunk, total, len, incl, sset, CS, R);
+  return phase;
+}
+
 template <int ESZ, bool PAGED, bool MODEL>
 __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
   constexpr int G = 16 / ESZ;
@@ -1025,12 +1261,18 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
   // most one word, an escaped position adds at most ESZ raw words.
   constexpr uint32_t kRoomPlain = kEmitBytes - 2 * G;
   constexpr uint32_t kRoomEsc = kEmitBytes - 2 * G * (1 + ESZ);
-  uint8_t* const smem = g_smem;
-  // stage the 32 encoder tables (8-byte entries)
+  // stage the 32 encoder tables (8-byte entries), every copy in flight at once
   for (uint32_t k = threadIdx.x; k < kKvTables * 256; k += blockDim.x) {
     const uint32_t t = k >> 8, sidx = k & 255;
-    *reinterpret_cast<uint2*>(smem + t * kEncTabStride + sidx * 8) =
-        reinterpret_cast<const uint2*>(a.tables + (uint64_t)t * SKV_TABLE_STRIDE + SKV_TABLE_ENC_OFF)[sidx];
+    if (SKV_SMEM_OK(t * kEncTabStride + sidx * 8, 8, kSiteSmemStore))
+      cp_async_8(t * kEncTabStride + sidx * 8, a.tables + (uint64_t)t * SKV_TABLE_STRIDE + SKV_TABLE_ENC_OFF + sidx * 8);
+  }
+  cp_async_wait_all();
+  // a warp's word buffers double as placement staging slots; its mbarriers
+  // follow all the word buffers
+  if ((threadIdx.x & 31) < kCpSlots) {
+    mbar_init(smem_addr(g_smem) + enc_bars_at(threadIdx.x >> 5, blockDim.x) + 8 * (threadIdx.x & 31), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
   const uint32_t tid = threadIdx.x & 31;
@@ -1047,13 +1289,14 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
   // one; by then its predecessors have published their totals, so placing it
   // rarely waits.
   unsigned long long pend = ~0ull, pend_total = 0;
-  uint32_t pend_len = 0, pend_incl = 0, set = 0;
+  uint32_t pend_len = 0, pend_incl = 0, set = 0, phase = 0;
   while (true) {
     unsigned long long chunk = 0;
     if (tid == 0) chunk = atomicAdd(a.ticket, 1ull);
     chunk = __shfl_sync(0xFFFFFFFFu, chunk, 0);
     if (chunk >= a.n_chunks) {
-      if (pend != ~0ull) place_chunk(a, pend, pend_total, pend_len, pend_incl, warp_gid * 2 + (set ^ 1u), CS, R);
+      if (pend != ~0ull)
+        place_pending(a, pend, pend_total, pend_len, pend_incl, warp_gid * 2 + (set ^ 1u), CS, R, true, phase);
       break;
     }
     uint8_t* const my_slot_end =
@@ -1234,7 +1477,11 @@ __global__ void __launch_bounds__(kEncThreads, 1) k_encode_kv(CodecArgs a) {
     }
     const unsigned long long total = __shfl_sync(0xFFFFFFFFu, incl, 31);
     chunk_publish(a.chunk_state, chunk, total);
-    if (pend != ~0ull) place_chunk(a, pend, pend_total, pend_len, pend_incl, warp_gid * 2 + (set ^ 1u), CS, R);
+    if (pend != ~0ull) {
+      phase = place_pending(a, pend, pend_total, pend_len, pend_incl, warp_gid * 2 + (set ^ 1u), CS, R,
+                            chunk >= a.last_wave, phase);
+      if (phase & kPlaceFailed) return;   // flagged; the warp's copies are waited for
+    }
     pend = chunk;
     pend_total = total;
     pend_len = len;
@@ -1292,12 +1539,13 @@ __global__ void __launch_bounds__(dec_threads(PAGED, MODEL), 1) k_decode_kv(Code
   constexpr int G = 16 / ESZ;
   constexpr int SUB = ESZ == 1 ? 8 : 4;   // at most 32 / 24 stream bytes between refills
   constexpr uint32_t kBias = ESZ == 1 ? 0x7F7F7F7Fu : 0x007F007Fu;
-  uint8_t* const smem = g_smem;
+  // stage the 32 slot->symbol + decoder tables, every copy in flight at once
   for (uint32_t k = threadIdx.x; k < kKvTables * 1280; k += blockDim.x) {
     const uint32_t t = k / 1280, w = k % 1280;
-    reinterpret_cast<uint32_t*>(smem + t * kDecTabStride)[w] =
-        reinterpret_cast<const uint32_t*>(a.tables + (uint64_t)t * SKV_TABLE_STRIDE + SKV_TABLE_LUT_OFF)[w];
+    if (SKV_SMEM_OK(t * kDecTabStride + 4 * w, 4, kSiteSmemStore))
+      cp_async_4(t * kDecTabStride + 4 * w, a.tables + (uint64_t)t * SKV_TABLE_STRIDE + SKV_TABLE_LUT_OFF + 4 * w);
   }
+  cp_async_wait_all();
   __syncthreads();
   const uint32_t lane = threadIdx.x & 31;
   const uint32_t ring = kDecTabBytes + threadIdx.x * kRingStride;
@@ -1711,37 +1959,7 @@ constexpr uint32_t kUmSmem = kUmStages * kUmStage + 1024 + 256;
 // instruction descriptor (kind::f16): fp32 accumulator (bits 4-5 = 1), bf16 A
 // and B (bits 7-9, 10-12 = 1), both K-major, N / 8 at bit 17, M / 16 at bit 24
 constexpr uint32_t kUmIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((kUmBN >> 3) << 17) | ((kUmBM >> 4) << 24);
-constexpr uint64_t kUmWaitNs = 1000000000ull;                // ~1 s bound on every barrier wait
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.b32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-// wait for the phase of parity `parity` to complete; false after ~1 s
-__device__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  while (!mbar_try(bar, parity))
-    if (global_ns() - t0 > kUmWaitNs) return false;
-  return true;
-}
 // 2-D tile load (x = inner element index, y = row) completing on `bar`
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, uint32_t x, uint32_t y,
                                             uint32_t bar) {
@@ -2292,8 +2510,13 @@ static int encode_impl(const skv_params* p, const Paged* pg, const void* d_targe
     st = cuda_status(cudaMemsetAsync(ws + wl.state_off, 0, wl.total - wl.state_off, s));
     if (st != SKV_OK) return st;
     codec_grid(g.n_chunks, &blocks, &threads, kEncThreads);
-    const int smem_bytes = (int)(kEncTabBytes + (uint32_t)threads * kEmitBytes);
-    const uint32_t smax = kEncTabBytes + kEncThreads * kEmitBytes;
+    {
+      uint64_t coding_warps = (uint64_t)blocks * (threads / 32);
+      if (coding_warps > a.slot_warps) coding_warps = a.slot_warps;
+      a.last_wave = g.n_chunks > coding_warps ? g.n_chunks - coding_warps : 0;
+    }
+    const int smem_bytes = (int)enc_smem_bytes((uint32_t)threads);
+    const uint32_t smax = enc_smem_bytes(kEncThreads);
     if (pg) a.pg = *pg;
     auto run = [&](auto kern) -> int {
       int e = set_smem(kern, smax);
