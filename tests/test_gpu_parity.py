@@ -107,6 +107,29 @@ def test_small_bit_exact(nat, w):
     full_compare(nat, w)
 
 
+@pytest.mark.parametrize("off", [2, 6, 14])
+def test_stream_at_unaligned_addresses(nat, off):
+    """The stream need only be 2-byte aligned: written at an address 2, 6 or 14
+    bytes past a 16-byte boundary it holds the same bytes and offsets, and
+    nothing outside it is touched.  Lanes of 16 positions give about four chunks
+    per warp, so both chunk copies run (lane by lane before the last wave,
+    through the staging slots in it)."""
+    w = synth.WORKLOADS["qwen3-0.6b-1k-fp8"].scaled(n_layers=4, lane_syms=16)
+    codec = full_compare(nat, w)   # aligned stream == the oracle's
+    t, p, _ = synth.gen_workload(w, "cpu")   # the inputs full_compare coded
+    t, p = t.cuda(), p.cuda()
+    total = codec.n_bytes
+    ref, ref_off = codec.bitstream[:total].clone(), codec.lane_offsets.clone()
+    buf = torch.full((codec.cap + 32,), 0xCD, dtype=torch.uint8, device="cuda")
+    view = buf[off:off + codec.cap]
+    codec.lane_offsets.fill_(-1)
+    st, tot = nat.skv_encode(codec.p, t, p, codec.tables, codec.bins, view, codec.cap, codec.lane_offsets,
+                             codec.workspace, codec.workspace.numel(), codec.status, want_total=True)
+    assert st == nat.SKV_OK and codec.check() == nat.SKV_OK and tot == total
+    assert torch.equal(view[:total], ref) and torch.equal(codec.lane_offsets, ref_off)
+    assert bool((buf[:off] == 0xCD).all()) and bool((buf[off + total:] == 0xCD).all())
+
+
 def test_calibration_sums_and_histograms(nat):
     w = synth.WORKLOADS["qwen3-0.6b-1k-fp8"].scaled(n_layers=1, n_tokens=600)
     t, p, _ = synth.gen_workload(w, "cpu")
