@@ -1699,9 +1699,10 @@ __device__ __forceinline__ void coef_load(const CodecArgs& a, uint64_t p0, uint3
   const int16_t* q = reinterpret_cast<const int16_t*>(a.tgt);
   const float* mu = reinterpret_cast<const float*>(a.prd);
   if (ne == 8) {
-    R.m0 = __ldg(reinterpret_cast<const float4*>(mu + p0));
-    R.m1 = __ldg(reinterpret_cast<const float4*>(mu + p0) + 1);
-    R.q = with_q ? __ldg(reinterpret_cast<const uint4*>(q + p0)) : make_uint4(0, 0, 0, 0);
+    // streaming loads: read once, so that they do not push the tables out of L2
+    R.m0 = __ldcs(reinterpret_cast<const float4*>(mu + p0));
+    R.m1 = __ldcs(reinterpret_cast<const float4*>(mu + p0) + 1);
+    R.q = with_q ? __ldcs(reinterpret_cast<const uint4*>(q + p0)) : make_uint4(0, 0, 0, 0);
     return;
   }
   float mv[8];

@@ -433,6 +433,43 @@ def _adversarial(kind, dtype, n, seed):
 
 
 @pytest.mark.parametrize("dtype", [synth.FP8, synth.BF16])
+def test_long_and_short_lanes_in_one_chunk(nat, dtype):
+    """The first 16 channels of every token take uniformly random residuals (their
+    four lanes per chunk hold 1.3-2.8 KB, mostly escapes), the others residuals of
+    at most 2: chunks of 12-22 KB whose long lanes span several 1-KB staging
+    pieces.  GPU stream == oracle stream, exact decode."""
+    L, KV, H, T, D, K = 2, 2, 2, 700, 128, 1024
+    n = L * KV * H * T * D
+    rng = np.random.default_rng(7 + dtype)
+    hi, dt = (256, np.uint8) if dtype == synth.FP8 else (1 << 16, np.uint16)
+    t = rng.integers(0, hi, n)
+    p = np.clip(t + rng.integers(-2, 3, n), 0, hi - 1)
+    hot = (np.arange(n) % D) < 16
+    p[hot] = rng.integers(0, hi, int(hot.sum()))
+    tn, pn = t.astype(dt), p.astype(dt)
+    po = oracle.kv_params(dtype, L, KV, H, D, T, K, 256)
+    bins, _, _ = oracle.calibrate(po, tn, pn)
+    fr, cum = oracle.build_tables(po)
+    st, bs, offs = oracle.encode(po, fr, cum, bins, tn, pn)
+    assert st == oracle.OK
+    lens = np.diff(offs.astype(np.int64))
+    assert lens.max() > 1024 and np.diff(offs[::32].astype(np.int64)).max() <= 32768   # the shape meant
+    tdt = torch.uint8 if dtype == synth.FP8 else torch.int16
+    td = torch.from_numpy(tn.view(np.int16) if dtype == synth.BF16 else tn).to(tdt).cuda()
+    pd = torch.from_numpy(pn.view(np.int16) if dtype == synth.BF16 else pn).to(tdt).cuda()
+    codec = nat.Codec(nat.kv_params(dtype, L, KV, H, D, T, K, 256))
+    codec.calibrate(td, pd)
+    codec.build_tables()
+    total = codec.encode(td, pd)
+    assert codec.check() == nat.SKV_OK and total == bs.size
+    assert np.array_equal(codec.bitstream[:total].cpu().numpy(), bs)
+    assert np.array_equal(codec.lane_offsets.cpu().numpy().astype(np.uint64), offs)
+    out = torch.empty_like(td)
+    codec.decode(pd, out)
+    assert codec.check() == nat.SKV_OK and torch.equal(out, td)
+
+
+@pytest.mark.parametrize("dtype", [synth.FP8, synth.BF16])
 @pytest.mark.parametrize("kind", ["uniform", "nan", "signflip", "extremes", "mixture"])
 def test_adversarial_bit_exact(nat, dtype, kind):
     """escape-heavy and special-value inputs: GPU stream == oracle stream, exact decode"""
