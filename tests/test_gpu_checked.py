@@ -87,3 +87,12 @@ def test_checked_corrupt_streams_and_models(nat):
     codec.decode(pd, out)
     assert codec.check() == nat.SKV_OK and torch.equal(out, td)
     _no_failures(nat)
+
+
+def test_checked_both_chunk_copies(nat):
+    """many short chunks per warp (16-position lanes): early chunks are placed by
+    the lane-by-lane copy, the last wave through the staging slots; no check fails
+    and the stream equals the oracle's"""
+    from test_gpu_parity import full_compare
+    full_compare(nat, synth.WORKLOADS["qwen3-0.6b-1k-fp8"].scaled(n_layers=4, lane_syms=16))
+    _no_failures(nat)
