@@ -436,10 +436,11 @@ def e2e(args, w, codec, tgt, prd, cal, out, stream, dev, total):
     import torch
     from lossless_kv_cache_fp8_gb300 import native, pipeline, synth
     try:
-        h_t = torch.empty(tgt.shape, dtype=tgt.dtype, pin_memory=True)
-        h_p = torch.empty(prd.shape, dtype=prd.dtype, pin_memory=True)
-        h_bs = torch.empty(int(total * 1.05) + 4096, dtype=torch.uint8, pin_memory=True)
-        h_out = torch.empty(tgt.shape, dtype=tgt.dtype, pin_memory=True) if w.dtype != synth.COEF else None
+        # page-locked host buffers backed by huge pages (see pipeline.pinned_empty)
+        h_t = pipeline.pinned_empty(tgt.shape, tgt.dtype)
+        h_p = pipeline.pinned_empty(prd.shape, prd.dtype)
+        h_bs = pipeline.pinned_empty((int(total * 1.05) + 4096,), torch.uint8)
+        h_out = pipeline.pinned_empty(tgt.shape, tgt.dtype) if w.dtype != synth.COEF else None
     except RuntimeError as e:
         return {"value": None, "unit": "GB/s", "error": f"pinned host allocation failed: {e}"[:200]}
     h_t.copy_(tgt)
