@@ -80,3 +80,31 @@ def test_host_calls_report_capacity_and_corruption(nat):
     assert e.value.status == nat.SKV_ERR_CORRUPT
     pipe.decode(h_bs, n, h_off, h_p, h_out)
     assert torch.equal(h_out, t.cpu())
+
+
+def test_pipeline_exponent_model_in_huge_page_buffers(nat):
+    """the exponent residual model through the host calls, with the host buffers
+    from pipeline.pinned_empty (huge-page backed, registered): equal to one call"""
+    from lossless_kv_cache_fp8_gb300 import pipeline
+    w = synth.WORKLOADS["qwen3-0.6b-1k-fp8"].scaled(n_layers=4, n_tokens=600)
+    params = nat.params_for(w, model=nat.SKV_MODEL_EXPONENT)
+    t, p, c = synth.gen_workload(w, "cuda")
+    codec = nat.Codec(params)
+    codec.calibrate(t, c)
+    codec.build_tables()
+    total = codec.encode(t, p)
+    assert codec.check() == nat.SKV_OK
+    h_t = pipeline.pinned_empty(t.shape, t.dtype)
+    h_p = pipeline.pinned_empty(p.shape, p.dtype)
+    h_bs = pipeline.pinned_empty((codec.cap,), torch.uint8)
+    h_off = pipeline.pinned_empty(tuple(codec.lane_offsets.shape), torch.int64)
+    h_out = pipeline.pinned_empty(t.shape, t.dtype)
+    assert h_t.is_pinned() and h_out.is_pinned() and h_t.shape == t.shape and h_t.dtype == t.dtype
+    h_t.copy_(t)
+    h_p.copy_(p)
+    pipe = pipeline.HostPipeline(params, group_layers=3)
+    n = pipe.run(h_t, h_p, h_bs, h_off, decode_into=h_out)
+    assert pipe.check() == nat.SKV_OK and n == total
+    assert torch.equal(h_bs[:n], codec.bitstream[:n].cpu())
+    assert torch.equal(h_off, codec.lane_offsets.cpu())
+    assert torch.equal(h_out, t.cpu())
