@@ -86,10 +86,9 @@ _HOST_BUFFERS = []   # (address, bytes) of the registered mappings (kept until t
 def pinned_empty(shape, dtype):
     """A host tensor in page-locked memory backed by transparent huge pages where
     the kernel offers them (an anonymous mapping advised MADV_HUGEPAGE, touched,
-    then registered with cudaHostRegister).  Copies of caches of tens of GB from
-    such memory keep the host link's full rate; ordinary page-locked allocations
-    of that size were measured at under half of it on some hosts (fragmented
-    small pages).  Falls back to torch's pinned allocation if the mapping or the
+    then registered with cudaHostRegister), for caches of tens of GB that cross
+    the host link: huge pages keep the device's address translation for the
+    copies cheap.  Falls back to torch's pinned allocation if the mapping or the
     registration fails.  The memory lives until the process exits."""
     import ctypes
     import ctypes.util
