@@ -87,8 +87,8 @@ def pinned_empty(shape, dtype):
     """A host tensor in page-locked memory backed by transparent huge pages where
     the kernel offers them (an anonymous mapping advised MADV_HUGEPAGE, touched,
     then registered with cudaHostRegister), for caches of tens of GB that cross
-    the host link: huge pages keep the device's address translation for the
-    copies cheap.  Falls back to torch's pinned allocation if the mapping or the
+    the host link (huge pages: far fewer page mappings behind each copy).
+    Falls back to torch's pinned allocation if the mapping or the
     registration fails.  The memory lives until the process exits."""
     import ctypes
     import ctypes.util
